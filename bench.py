@@ -1,0 +1,399 @@
+"""Benchmark: forward pass of the Mixtral-shaped MoE layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+A step is one whole layer forward (route -> permute -> GEMM0+SwiGLU ->
+GEMM1+scatter -> combine) over one batch of T tokens, through the C ABI
+(moe_layer_forward). Inputs are seeded synthetic bf16 tensors of the
+configuration's shape, resident in HBM before timing. L2 is flushed (a
+256 MiB write) between timed steps; each step is timed with CUDA events on
+the launching stream. Prints one JSON line (rank 0).
+
+Multi-GPU: the layer's tokens are independent, so N GPUs run N independent
+replicas of the workload (weak scaling, no collective on the data path);
+the barrier/max-over-ranks timing follows the launcher's contract.
+
+--impl reference times the CPU oracle on a bounded sample of the same
+workload (the only place besides the cpu_baseline field where the benchmark
+runs the oracle).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from token_dispatch_grouped_moe_gb300.configs import CONFIGS  # noqa: E402
+
+METRIC = "MoE layer fwd bf16 TFLOP/s & tokens/s on 1 GB300; % of tensor peak / HBM BW"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def make_workload(cfg, device):
+    import torch
+    from token_dispatch_grouped_moe_gb300.inputs import make_inputs
+    inp = make_inputs(cfg.T, cfg.H, cfg.F, cfg.E, Fs=cfg.Fs, seed=cfg.seed)
+    return inp, {n: v.to(device) for n, v in inp.items()}
+
+
+def roofline_stage_bytes(cfg):
+    """Algorithmic bytes of the HBM-bound stages (per launch)."""
+    T, H, E, k, R = cfg.T, cfg.H, cfg.E, cfg.k, cfg.R
+    n_slots = k + (1 if cfg.Fs else 0)
+    return {
+        "route": T * H * 2 + H * E * 2 + T * k * 8,
+        "combine": n_slots * T * H * 4 + T * H * 2,
+        "permute_index": R * 4 * 4 + E * 8,
+    }
+
+
+def cpu_baseline(cfg, inp, budget_s=15.0, max_tokens=None):
+    """The oracle, as it stands, on a bounded sample of this workload's tokens."""
+    from oracle.oracle import Oracle
+    from token_dispatch_grouped_moe_gb300.inputs import bf16_bits
+    O = Oracle()
+    b = {n: bf16_bits(v) for n, v in inp.items()}
+    flops_per_token = cfg.flops() / cfg.T
+
+    def run(n):
+        xs = b["x"][:n]
+        t0 = time.perf_counter()
+        _, idx, w = O.route(xs, b["Wg"], cfg.k)
+        O.layer_rows(np.arange(n, dtype=np.int64), idx, w, xs, b["W1"], b["W3"], b["W2"],
+                     b.get("W1s"), b.get("W3s"), b.get("W2s"))
+        return time.perf_counter() - t0
+
+    n = max(1, min(O.num_threads(), cfg.T))
+    dt = run(n)
+    # grow the sample to about budget_s of CPU work
+    target = int(n * budget_s / max(dt, 1e-3))
+    if max_tokens:
+        target = min(target, max_tokens)
+    target = max(n, min(cfg.T, target))
+    if target > n:
+        n = target
+        dt = run(n)
+    return {"value": n * flops_per_token / dt / 1e12, "unit": "TFLOP/s", "cores": O.num_threads(),
+            "kind": "oracle", "tokens_per_s": n / dt,
+            "sample": f"first {n} of {cfg.T} tokens of the {cfg.name} workload (route + FFN + combine)"}
+
+
+def bench_ours(args, cfg):
+    import torch
+    from token_dispatch_grouped_moe_gb300 import build as cuda_build
+    from token_dispatch_grouped_moe_gb300 import lib
+
+    rank, world, local = dist_env()
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    if not os.path.exists(lib.LIB_PATH):
+        cuda_build.build()
+    lib.load()
+
+    inp, g = make_workload(cfg, device)
+    dims = lib.make_dims(cfg.T, cfg.H, cfg.F, cfg.E, cfg.k, cfg.Fs)
+    ws = lib.workspace(dims, device=device)
+    out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    names = ["before_route", "before_permute", "before_gemm0", "before_gemm1", "before_shared",
+             "before_combine", "after_combine"]
+
+    def new_events():
+        # torch creates the CUDA event on its first record; record once so the
+        # raw handle exists before the library records it between stages
+        evs = [torch.cuda.Event(enable_timing=True) for _ in names]
+        for e in evs:
+            e.record(stream)
+        se = lib.StageEvents(*[lib.ctypes.c_void_p(e.cuda_event) for e in evs])
+        return evs, se
+
+    def step(se=None):
+        lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws, W1s=g.get("W1s"),
+                          W3s=g.get("W3s"), W2s=g.get("W2s"), out=out, events=se)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if lib.check(ws) != lib.MOE_OK:
+        raise RuntimeError("device error during warm-up")
+
+    recs = [new_events() for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(1)
+        step(recs[i][1])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    if lib.check(ws) != lib.MOE_OK:
+        raise RuntimeError("device error during timing")
+
+    stage_ms = {n: [] for n in ("route", "permute", "gemm0", "gemm1", "shared", "combine")}
+    step_ms = []
+    for evs, _ in recs:
+        t = [evs[0].elapsed_time(e) for e in evs]
+        step_ms.append(t[-1])
+        for j, n in enumerate(stage_ms):
+            stage_ms[n].append(t[j + 1] - t[j])
+    ms = float(np.sum(step_ms)) / args.steps
+    if world > 1:
+        tt = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # end to end through the C ABI with host buffers: x H2D, layer, out D2H
+    x_host = inp["x"].pin_memory()
+    out_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(g["x"])
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        x_dev.copy_(x_host, non_blocking=True)
+        lib.layer_forward(dims, x_dev, g["Wg"], g["W1"], g["W3"], g["W2"], ws, W1s=g.get("W1s"),
+                          W3s=g.get("W3s"), W2s=g.get("W2s"), out=out)
+        out_host.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    e2e = float(np.mean(e2e_ms))
+    if world > 1:
+        tt = torch.tensor([e2e], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e = float(tt.item())
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return None
+
+    peaks = measured_peaks()
+    flops = cfg.flops()
+    gemm0_ms = float(np.mean(stage_ms["gemm0"]))
+    gemm0_flops = 4 * cfg.R * cfg.H * cfg.F
+    achieved = gemm0_flops / (gemm0_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    stage_summary = {n: round(float(np.mean(v)), 4) for n, v in stage_ms.items()}
+    by = roofline_stage_bytes(cfg)
+    stage_roofline = {
+        "gemm0": {"tflops": round(achieved, 1), "frac": round(achieved / peak, 4)},
+        "gemm1": {"tflops": round(2 * cfg.R * cfg.F * cfg.H / (np.mean(stage_ms["gemm1"]) * 1e-3) / 1e12, 1)},
+        "route": {"gbs": round(by["route"] / (np.mean(stage_ms["route"]) * 1e-3) / 1e9, 1)},
+        "combine": {"gbs": round(by["combine"] / (np.mean(stage_ms["combine"]) * 1e-3) / 1e9, 1)},
+    }
+    stage_roofline["gemm1"]["frac"] = round(stage_roofline["gemm1"]["tflops"] / peak, 4)
+    stage_roofline["route"]["frac"] = round(stage_roofline["route"]["gbs"] / peaks["hbm_gbs"], 4)
+    stage_roofline["combine"]["frac"] = round(stage_roofline["combine"]["gbs"] / peaks["hbm_gbs"], 4)
+
+    value = world * flops / (ms * 1e-3) / 1e12
+    launches_per_step = 1 + 2 + 2 + (2 if cfg.Fs else 0) + 1
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "tokens_per_s": round(world * cfg.T / (ms * 1e-3), 1),
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded randn: x sigma 1, weights sigma 0.02, bf16)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} F={cfg.F} E={cfg.E} top-{cfg.k}"
+                               + (f" shared F={cfg.Fs}" if cfg.Fs else "") + " SwiGLU",
+                   "T": cfg.T, "H": cfg.H, "F": cfg.F, "E": cfg.E, "k": cfg.k, "F_shared": cfg.Fs,
+                   "l2": "flushed (256 MiB write) between timed steps",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": "grouped GEMM0 + SwiGLU (tcgen05)",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"},
+        "stage_ms": stage_summary,
+        "stage_roofline": stage_roofline,
+        "e2e": {"value": round(world * flops / (e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": cfg.T * cfg.H * 2,
+                "d2h_bytes_per_step": cfg.T * cfg.H * 2},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, inp, budget_s=args.cpu_budget)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line
+
+
+def bench_reference(args, cfg):
+    """The oracle (CPU) as the reference arm: each step is a bounded sample."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    from oracle.oracle import Oracle
+    from token_dispatch_grouped_moe_gb300.inputs import bf16_bits, make_inputs
+    O = Oracle()
+    inp = make_inputs(cfg.T, cfg.H, cfg.F, cfg.E, Fs=cfg.Fs, seed=cfg.seed)
+    b = {n: bf16_bits(v) for n, v in inp.items()}
+    n_tok = max(1, min(cfg.T, args.ref_tokens))
+    flops_per_token = cfg.flops() / cfg.T
+
+    def step(i):
+        lo = (i * n_tok) % cfg.T
+        xs = b["x"][lo:lo + n_tok]
+        _, idx, w = O.route(xs, b["Wg"], cfg.k)
+        O.layer_rows(np.arange(xs.shape[0], dtype=np.int64), idx, w, xs, b["W1"], b["W3"], b["W2"],
+                     b.get("W1s"), b.get("W3s"), b.get("W2s"))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n_tok * flops_per_token / dt / 1e12
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "tokens_per_s": round(n_tok / dt, 3),
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 FFN / f32 routing (CPU oracle)",
+        "data": "synthetic (seeded randn: x sigma 1, weights sigma 0.02, bf16)",
+        "config": {"workload": f"{cfg.name}: T={cfg.T} H={cfg.H} F={cfg.F} E={cfg.E} top-{cfg.k}",
+                   "T": cfg.T, "H": cfg.H, "F": cfg.F, "E": cfg.E, "k": cfg.k, "F_shared": cfg.Fs},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": O.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{n_tok} of {cfg.T} tokens per step of the {cfg.name} workload"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="mixtral", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
+    ap.add_argument("--ref-tokens", type=int, default=64, help="oracle tokens per reference step")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
+    cfg = CONFIGS[args.config]
+    line = bench_reference(args, cfg) if args.impl == "reference" else bench_ours(args, cfg)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,187 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) MoE FFN layer forward.
+ *
+ * The layer: top-k routing, dispatch of the routed (token, expert) pairs into
+ * per-expert groups, a SwiGLU expert FFN per group (GEMM0 + SwiGLU split
+ * along the token dimension M, GEMM1 split along the hidden dimension N),
+ * and the gate-weighted combine back to token order. The parts are those
+ * named in the DisagMoE summary (gist.science, "Resumo Tecnico: DisagMoE",
+ * section 2.2, "Alinhamento de Estagios": top-k experts, dispatch, combine)
+ * and on the COMET page (nav.superapi.store/en/comet, "COMET's Technical
+ * Principles", "Tensor Decomposition": Layer 0 split along M, Layer 1 along
+ * N). The pages give no formulas; the readings used here are:
+ *   - logits l[t,e] = sum_h x[t,h] Wg[h,e] in fp32 in one canonical order
+ *     (8-element chunks, chunk c on lane c mod 32, fma in increasing h, then
+ *     an xor butterfly over the 32 lane sums with strides 16, 8, 4, 2, 1),
+ *     plus bias[e] when a bias is given;
+ *   - top-k on the logits, descending, ties to the lower expert id; the rank
+ *     of an expert is its selection position;
+ *   - gate weights = softmax over the k selected logits;
+ *   - expert e: y = (silu(x W1[e]) * (x W3[e])) W2[e], silu(a) = a/(1+e^-a);
+ *   - out[t] = sum over ranks j = 0..k-1 (in that order) of w[t,j] y_j,
+ *     plus the always-on shared expert (weight 1) when F_shared > 0.
+ *
+ * Conventions (every entry point):
+ *   - Tensors are row-major and contiguous: x[T,H], Wg[H,E], W1/W3[E,H,F],
+ *     W2[E,F,H]; shared expert W1s/W3s[H,Fs], W2s[Fs,H]. bf16 tensors are
+ *     passed as moe_bf16 (raw bf16 bits).
+ *   - Every pointer is a device pointer owned by the caller; the library
+ *     allocates no memory and keeps no per-call state. Scratch memory is the
+ *     caller's workspace `ws` of at least moe_workspace_size(dims) bytes,
+ *     256-byte aligned. Two calls that share a workspace must not overlap.
+ *   - Calls are asynchronous on `stream`. Argument checks run on the host
+ *     before any launch and return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED
+ *     / MOE_ERR_WORKSPACE without launching. A launch failure returns
+ *     MOE_ERR_CUDA. Errors found on the device (an expert id outside
+ *     [0, E), a bounded wait that ran out) are OR-ed into the error word at
+ *     the start of `ws` and read by moe_check(); with the environment
+ *     variable MOE_DEBUG=1 every entry point synchronises and checks.
+ *   - Supported shapes (else MOE_ERR_UNSUPPORTED): 1 <= k <= min(E, 8),
+ *     E <= 256, H and F (and F_shared) multiples of 64, T*k < 2^31.
+ *     T == 0 is a valid no-op. Pointers must be 16-byte aligned.
+ *   - Results are bit-identical from run to run (no float atomics).
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_bf16;                 /* raw bf16 bits */
+typedef struct CUstream_st* moe_stream_t;  /* the same type as cudaStream_t */
+typedef struct CUevent_st* moe_event_t;    /* the same type as cudaEvent_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* null pointer, negative size, bad id (device) */
+    MOE_ERR_UNSUPPORTED = 2,   /* shape outside the supported set */
+    MOE_ERR_WORKSPACE = 3,     /* workspace missing, too small or misaligned */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime / driver call failed */
+    MOE_ERR_TIMEOUT = 5,       /* a bounded device wait ran out (device) */
+    MOE_ERR_DEVICE_BOUNDS = 6  /* a device index check failed (device) */
+} moe_status;
+
+typedef struct {
+    int64_t T;         /* tokens */
+    int32_t H;         /* hidden size */
+    int32_t F;         /* expert FFN width */
+    int32_t E;         /* routed experts */
+    int32_t k;         /* experts per token */
+    int32_t F_shared;  /* shared expert FFN width; 0 = no shared expert */
+} moe_dims;
+
+/* Optional per-stage timing: each non-null event is recorded on the stream
+ * at that point of moe_layer_forward. */
+typedef struct {
+    moe_event_t before_route;
+    moe_event_t before_permute;
+    moe_event_t before_gemm0;      /* routed GEMM0 + SwiGLU */
+    moe_event_t before_gemm1;      /* routed GEMM1 + weighted scatter */
+    moe_event_t before_shared;     /* shared-expert GEMM0 + GEMM1 (if any) */
+    moe_event_t before_combine;
+    moe_event_t after_combine;
+} moe_stage_events;
+
+/* Optional routing outputs of moe_layer_forward; each null field is kept in
+ * the workspace instead. Sizes: [T*k], [T*k], [E], [E+1], [T*k], [T*k]. */
+typedef struct {
+    int32_t* topk_idx;
+    float* topk_w;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* src_row;
+    int32_t* inv_pos;
+} moe_routing_out;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int moe_version(void);
+
+/* Text for a status code. Never null. */
+const char* moe_status_string(int status);
+
+/* Workspace bytes that every entry point below accepts for `dims`.
+ * Returns 0 for invalid dims. */
+size_t moe_workspace_size(const moe_dims* dims);
+
+/* Synchronises `stream`, reads and clears the device error word at the start
+ * of `ws`, and returns the status it holds (MOE_OK if none). */
+moe_status moe_check(void* ws, moe_stream_t stream);
+
+/*
+ * Router (top-k gating).
+ * In:  x[T,H], Wg[H,E] (bf16); bias[E] (f32, may be null).
+ * Out: topk_idx[T,k] (int32, expert ids in rank order), topk_w[T,k] (f32,
+ *      the softmax of the selected logits, in rank order).
+ * The logits are computed in the canonical fp32 order given above, so the ids
+ * are bit-exact against any implementation of that order.
+ */
+moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg, const float* bias,
+                     int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
+/*
+ * Dispatch: stable counting sort of the R = T*k assignments f = t*k + j by
+ * expert id topk_idx[f] (the "dispatch" of the DisagMoE summary, 2.2).
+ * In:  topk_idx[R] (int32).
+ * Out: counts[E]; offsets[E+1] (exclusive scan, offsets[E] = R);
+ *      src_row[R] (src_row[p] = f, experts in increasing order, f increasing
+ *      within an expert); inv_pos[R] (inv_pos[f] = p).
+ *      x_perm[R,H] (bf16, may be null): x_perm[p] = x[src_row[p] / k]; x
+ *      must be given when x_perm is.
+ * An id outside [0, E) sets MOE_ERR_INVALID_ARG in the device error word and
+ * that assignment is skipped (no out-of-bounds write).
+ * Also writes the GEMM tile table into `ws` for a later moe_expert_ffn /
+ * moe_layer_forward on the same workspace.
+ */
+moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* counts,
+                       int32_t* offsets, int32_t* src_row, int32_t* inv_pos, const moe_bf16* x,
+                       moe_bf16* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Expert FFN over the dispatched groups: for every position p of expert e
+ * (offsets[e] <= p < offsets[e+1]) with f = src_row[p], t = f / k, j = f % k:
+ *   h[p]      = silu(x[t] W1[e]) * (x[t] W3[e])     (GEMM0 + SwiGLU, h in bf16)
+ *   slot[j,t] = w * (h[p] W2[e])                    (GEMM1 + weighted scatter)
+ * with w = topk_w[f], or 1 when topk_w is null.
+ * In:  x[T,H]; src_row[R] (null = identity: f = p); offsets[E+1] (null = one
+ *      group holding all R rows; then E must be 1); W1/W3[E,H,F], W2[E,F,H].
+ * Out: slot[k,T,H] (f32). Every (j, t) slot is written exactly once.
+ * Call with dims {T, H, F=Fs, E=1, k=1} and null src_row/offsets/topk_w to
+ * run a dense (shared) expert into slot[0].
+ */
+moe_status moe_expert_ffn(const moe_dims* dims, const moe_bf16* x, const int32_t* src_row,
+                          const int32_t* offsets, const moe_bf16* W1, const moe_bf16* W3,
+                          const moe_bf16* W2, const float* topk_w, float* slot, void* ws,
+                          size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Combine (the "combine" of the DisagMoE summary, 2.2): out[t,:] =
+ * bf16( ((slot[0,t,:] + slot[1,t,:]) + ...) + slot[n_slots-1,t,:] ), an fp32
+ * left fold in slot order, no atomics.
+ * In:  slot[n_slots,T,H] (f32), 1 <= n_slots <= 9.  Out: out[T,H] (bf16).
+ */
+moe_status moe_combine(const moe_dims* dims, const float* slot, int32_t n_slots, moe_bf16* out,
+                       moe_stream_t stream);
+
+/*
+ * The whole layer: route -> permute -> expert FFN (routed; then the shared
+ * expert when dims->F_shared > 0) -> combine.
+ * In:  x, Wg, bias (nullable), W1, W3, W2; W1s/W3s/W2s (needed iff F_shared > 0).
+ * Out: out[T,H] (bf16); routing (nullable) receives the routing tensors.
+ * events (nullable) are recorded at the stage boundaries.
+ */
+moe_status moe_layer_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg,
+                             const float* bias, const moe_bf16* W1, const moe_bf16* W3,
+                             const moe_bf16* W2, const moe_bf16* W1s, const moe_bf16* W3s,
+                             const moe_bf16* W2s, moe_bf16* out, const moe_routing_out* routing,
+                             void* ws, size_t ws_bytes, const moe_stage_events* events,
+                             moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

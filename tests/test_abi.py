@@ -1,0 +1,95 @@
+"""The C-ABI library: loads, exports what include/moe.h declares, validates
+arguments on the host (CPU only: no call here reaches a kernel launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from token_dispatch_grouped_moe_gb300 import build, lib
+    build.build()
+    return lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_match_header(L):
+    from token_dispatch_grouped_moe_gb300 import lib
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in moe.h but not exported"
+    assert sorted(lib.EXPORTS) == sorted(n for n in names if n in lib.EXPORTS)
+    assert set(lib.EXPORTS) <= set(names)
+
+
+def test_version_and_status_strings(L):
+    assert L.moe_version() >= 100
+    for code in range(0, 7):
+        s = L.moe_status_string(code).decode()
+        assert s.startswith("MOE_")
+    assert L.moe_status_string(99) == b"unknown moe_status"
+
+
+def test_workspace_size(L):
+    from token_dispatch_grouped_moe_gb300 import lib
+    d = lib.make_dims(8192, 4096, 14336, 8, 2)
+    n = lib.workspace_size(d)
+    # h (R*F bf16) + slot (k*T*H f32) dominate
+    assert n >= 16384 * 14336 * 2 + 2 * 8192 * 4096 * 4
+    assert n % 256 == 0
+    for bad in [lib.make_dims(-1, 64, 64, 8, 2), lib.make_dims(8, 60, 64, 8, 2),
+                lib.make_dims(8, 64, 64, 8, 9), lib.make_dims(8, 64, 64, 300, 2),
+                lib.make_dims(8, 64, 64, 2, 3)]:
+        assert lib.workspace_size(bad) == 0
+    assert L.moe_workspace_size(None) == 0
+
+
+def test_host_validation_without_launch(L):
+    """Errors found on the host return before any CUDA call."""
+    from token_dispatch_grouped_moe_gb300 import lib
+    dummy = ctypes.c_void_p(256)
+    null = None
+    # null dims
+    assert L.moe_route(None, dummy, dummy, null, dummy, dummy, null) == 1
+    # unsupported: H not a multiple of 64; k > 8; E > 256
+    for d, want in [(lib.make_dims(8, 96, 64, 8, 2), 2), (lib.make_dims(8, 64, 64, 16, 9), 2),
+                    (lib.make_dims(8, 64, 64, 300, 2), 2), (lib.make_dims(8, 64, 64, 4, 5), 1)]:
+        assert L.moe_route(ctypes.byref(d), dummy, dummy, null, dummy, dummy, null) == want
+    d = lib.make_dims(8, 64, 64, 8, 2)
+    # missing pointers
+    assert L.moe_route(ctypes.byref(d), null, dummy, null, dummy, dummy, null) == 1
+    # misaligned x
+    assert L.moe_route(ctypes.byref(d), ctypes.c_void_p(257), dummy, null, dummy, dummy, null) == 1
+    # workspace: null, misaligned, too small
+    need = lib.workspace_size(d)
+    args = [ctypes.byref(d), dummy, dummy, dummy, dummy, dummy, null, null]
+    assert L.moe_permute(*args, null, need, null) == 3
+    assert L.moe_permute(*args, ctypes.c_void_p(4096 + 16), need, null) == 3
+    assert L.moe_permute(*args, ctypes.c_void_p(4096), need - 1, null) == 3
+    # combine: slot count out of range
+    assert L.moe_combine(ctypes.byref(d), dummy, 0, dummy, null) == 1
+    assert L.moe_combine(ctypes.byref(d), dummy, 10, dummy, null) == 1
+    # shared expert weights required when F_shared > 0
+    ds = lib.make_dims(8, 64, 64, 8, 2, 64)
+    assert L.moe_layer_forward(ctypes.byref(ds), dummy, dummy, null, dummy, dummy, dummy, null, null,
+                               null, dummy, null, ctypes.c_void_p(4096), lib.workspace_size(ds), null,
+                               null) == 1
+
+
+def test_zero_tokens_is_noop_on_host(L):
+    """T = 0 returns MOE_OK before touching any pointer or the device."""
+    from token_dispatch_grouped_moe_gb300 import lib
+    d = lib.make_dims(0, 64, 64, 8, 2)
+    assert L.moe_route(ctypes.byref(d), None, None, None, None, None, None) == 0
+    assert L.moe_combine(ctypes.byref(d), None, 1, None, None) == 0

@@ -1,0 +1,202 @@
+"""CUDA path against the oracle, through the C ABI (GPU only).
+
+Integer results (top-k ids, counts, offsets, src_row, inv_pos) must match
+bit for bit. Gate weights: within 1e-5 relative. Layer output (bf16) against
+the oracle's fp64 output: max |out - ref| <= 2e-2 * rms(ref).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from token_dispatch_grouped_moe_gb300.configs import CONFIGS
+from token_dispatch_grouped_moe_gb300.inputs import bf16_bits, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_OUT = 2e-2       # max |out - ref| / rms(ref)
+TOL_W = 1e-5         # relative, gate weights
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from token_dispatch_grouped_moe_gb300 import build, lib as L
+    build.build()
+    L.load()
+    return L
+
+
+def zipf_bias():
+    vals = [float.fromhex(l.strip()) for l in open(os.path.join(GOLDEN, "zipf_bias_mixtral.txt"))
+            if l.strip() and not l.startswith("#")]
+    return np.array(vals, np.float32)
+
+
+def run_case(lib, oracle, T, H, F, E, k, Fs=0, seed=0, bias=None, sample=None, check_perm=True):
+    """Runs the layer on the GPU and the oracle on the CPU; returns stats."""
+    inp = make_inputs(T, H, F, E, Fs=Fs, seed=seed)
+    dev = torch.device("cuda")
+    g = {n: v.to(dev) for n, v in inp.items()}
+    b = {n: bf16_bits(v) for n, v in inp.items()}
+    bias_t = None if bias is None else torch.from_numpy(np.asarray(bias, np.float32)).to(dev)
+    dims = lib.make_dims(T, H, F, E, k, Fs)
+    ws = lib.workspace(dims, device=dev)
+    routing = lib.routing_buffers(dims, dev)
+    out = lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws, bias=bias_t,
+                            W1s=g.get("W1s"), W3s=g.get("W3s"), W2s=g.get("W2s"), routing=routing)
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+    # routing and dispatch: the oracle on every token
+    logits, idx, w = oracle.route(b["x"], b["Wg"], k, bias)
+    assert np.array_equal(routing.topk_idx.cpu().numpy(), idx), "top-k ids differ"
+    gw = routing.topk_w.cpu().numpy()
+    assert np.allclose(gw, w, rtol=TOL_W, atol=1e-7), f"gate weights differ: {np.max(np.abs(gw - w))}"
+    if check_perm:
+        counts, offsets, src_row, inv_pos = oracle.permute(idx, E)
+        assert np.array_equal(routing.counts.cpu().numpy(), counts)
+        assert np.array_equal(routing.offsets.cpu().numpy(), offsets)
+        assert np.array_equal(routing.src_row.cpu().numpy(), src_row)
+        assert np.array_equal(routing.inv_pos.cpu().numpy(), inv_pos)
+    # output rows: all tokens, or a seeded sample at large sizes
+    if sample is None or sample >= T:
+        tokens = np.arange(T, dtype=np.int64)
+    else:
+        rng = np.random.default_rng(seed + 99)
+        tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, sample, replace=False)]))
+    ref = oracle.layer_rows(tokens, idx, w, b["x"], b["W1"], b["W3"], b["W2"], b.get("W1s"),
+                            b.get("W3s"), b.get("W2s"))
+    o = out.float().cpu().numpy()[tokens].astype(np.float64)
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    err = float(np.max(np.abs(o - ref)))
+    assert err <= TOL_OUT * rms, f"max err {err:.4e} > {TOL_OUT} * rms {rms:.4e} (ratio {err / rms:.4f})"
+    return dict(err_ratio=err / rms, out=out, routing=routing, inputs=g, ws=ws, dims=dims)
+
+
+SMALL_CASES = {
+    # name: (T, H, F, E, k, Fs)
+    "tiny": (256, 512, 1024, 8, 2, 0),
+    "ragged": (1000, 512, 768, 8, 2, 0),
+    "f_tail": (77, 256, 320, 5, 3, 0),          # F % 128 == 64: half GEMM0 N tile; E not % 8
+    "h_tail_e64": (300, 192, 128, 64, 6, 0),    # H % 256 == 192: GEMM1 N tail; empty experts
+    "dense_e1": (130, 256, 192, 1, 1, 0),       # E = 1, k = 1: a dense SwiGLU FFN
+    "k_eq_e": (64, 128, 128, 4, 4, 0),          # every expert chosen by every token
+    "shared": (200, 256, 128, 16, 4, 384),      # always-on shared expert
+    "one_token": (1, 128, 64, 8, 2, 0),
+    "three_tokens": (3, 64, 64, 3, 2, 0),
+    "seventeen": (17, 320, 192, 2, 1, 0),
+    "e256": (64, 128, 64, 256, 8, 0),           # the largest supported E and k
+}
+
+
+@pytest.mark.parametrize("name", list(SMALL_CASES))
+def test_small_case(lib, oracle, name):
+    T, H, F, E, k, Fs = SMALL_CASES[name]
+    run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=1)
+
+
+def test_zipf_bias_small(lib, oracle):
+    """Biased (skewed) routing on a Mixtral-like E=8 top-2 layer at small H/F."""
+    bias = zipf_bias()
+    r = run_case(lib, oracle, 2048, 512, 256, 8, 2, seed=0, bias=bias * 0.5)
+    counts = r["routing"].counts.cpu().numpy()
+    assert counts[0] > counts[-1]
+
+
+def test_deterministic(lib, oracle):
+    T, H, F, E, k = 700, 256, 256, 8, 2
+    inp = make_inputs(T, H, F, E, seed=5)
+    g = {n: v.cuda() for n, v in inp.items()}
+    dims = lib.make_dims(T, H, F, E, k)
+    ws = lib.workspace(dims)
+    o1 = lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws).clone()
+    o2 = lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2)
+
+
+def test_stage_api_matches_layer(lib, oracle):
+    """route -> permute -> expert_ffn -> combine equals moe_layer_forward bit for bit;
+    x_perm equals x gathered by src_row."""
+    T, H, F, E, k, Fs = 300, 256, 192, 8, 2, 128
+    inp = make_inputs(T, H, F, E, Fs=Fs, seed=7)
+    g = {n: v.cuda() for n, v in inp.items()}
+    dims = lib.make_dims(T, H, F, E, k, Fs)
+    ws = lib.workspace(dims)
+    ref = lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws, W1s=g["W1s"],
+                            W3s=g["W3s"], W2s=g["W2s"]).clone()
+    idx, w = lib.route(dims, g["x"], g["Wg"])
+    counts, offsets, src_row, inv_pos, x_perm = lib.permute(dims, idx, ws, x=g["x"], want_x_perm=True)
+    slot = torch.empty(k + 1, T, H, dtype=torch.float32, device="cuda")
+    lib.expert_ffn(dims, g["x"], src_row, offsets, g["W1"], g["W3"], g["W2"], w, ws, slot=slot[:k])
+    sd = lib.make_dims(T, H, Fs, 1, 1)
+    sws = lib.workspace(sd)
+    lib.expert_ffn(sd, g["x"], None, None, g["W1s"], g["W3s"], g["W2s"], None, sws, slot=slot[k:])
+    out = lib.combine(dims, slot)
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+    assert torch.equal(out, ref)
+    tok = (src_row.long() // k)
+    assert torch.equal(x_perm, g["x"][tok])
+
+
+def test_bad_expert_id_reported(lib):
+    """An id outside [0, E) is reported through the device error word; the
+    other assignments are still dispatched; nothing is written out of bounds."""
+    T, E, k = 64, 8, 2
+    dims = lib.make_dims(T, 64, 64, E, k)
+    ws = lib.workspace(dims)
+    idx = torch.randint(0, E, (T, k), dtype=torch.int32, device="cuda")
+    idx[5, 1] = E + 3
+    idx[9, 0] = -2
+    guard = torch.full((2 * T * k + 64,), -7, dtype=torch.int32, device="cuda")
+    src_row = guard[32:32 + T * k]
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    inv_pos = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    import ctypes
+    st = lib.load().moe_permute(ctypes.byref(dims), ctypes.c_void_p(idx.data_ptr()),
+                                ctypes.c_void_p(counts.data_ptr()), ctypes.c_void_p(offsets.data_ptr()),
+                                ctypes.c_void_p(src_row.data_ptr()), ctypes.c_void_p(inv_pos.data_ptr()),
+                                None, None, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == lib.MOE_OK
+    assert lib.check(ws) == 1   # MOE_ERR_INVALID_ARG from the device
+    assert lib.check(ws) == lib.MOE_OK   # cleared by the read
+    assert int(counts.sum()) == T * k - 2
+    g = guard.cpu().numpy()
+    assert np.all(g[:32] == -7) and np.all(g[32 + T * k:] == -7)
+
+
+def test_zero_tokens(lib):
+    dims = lib.make_dims(0, 128, 64, 8, 2)
+    ws = lib.workspace(dims)
+    x = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    W = torch.empty(1, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty(0, 128, dtype=torch.bfloat16, device="cuda")
+    Wg = torch.zeros(128, 8, dtype=torch.bfloat16, device="cuda")
+    lib.layer_forward(dims, x, Wg, W, W, W, ws, out=out)
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+
+
+# ----------------------------------------------------------- full sizes --
+
+FULL = ["mixtral", "qwen2", "dsk-1k", "dsk-4k", "dsk-16k", "dsk-32k", "mixtral-zipf"]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", FULL)
+def test_full_config(lib, oracle, name):
+    """The configurations at full size, launched as the benchmark launches
+    them. Routing and dispatch are compared on every token; the output on a
+    seeded sample of tokens (rows are independent, so the sample is exact)."""
+    c = CONFIGS[name]
+    bias = zipf_bias() if c.zipf else None
+    r = run_case(lib, oracle, c.T, c.H, c.F, c.E, c.k, Fs=c.Fs, seed=c.seed, bias=bias, sample=48)
+    if c.zipf:
+        share = r["routing"].counts.cpu().numpy() / c.R
+        assert 0.38 <= share[0] <= 0.45

@@ -1,0 +1,399 @@
+// api.cu -- the C ABI of include/moe.h: argument checks, workspace layout,
+// TMA descriptors and the launch sequence of the layer. Host code only.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe.h"
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kVersion = 100;   // 0.1.0
+constexpr int kMaxDevices = 64;
+
+// ------------------------------------------------------------ device info --
+
+std::atomic<int> g_num_sms[kMaxDevices];
+
+int num_sms_current()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    int n = g_num_sms[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return -1;
+    g_num_sms[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+bool debug_mode()
+{
+    static const bool on = [] {
+        const char* v = std::getenv("MOE_DEBUG");
+        return v && v[0] && std::strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
+// ---------------------------------------------------------- tensor maps --
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2D bf16 tensor [outer, inner] (inner contiguous), box {64, box_outer},
+// 128-byte swizzle; out-of-bounds elements read as zero.
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ workspace --
+
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct Layout {
+    size_t err, tile, hist, idx, w, counts, offsets, src, inv, h, hs, slot, total;
+};
+
+Layout layout_of(const moe_dims& d)
+{
+    const size_t T = (size_t)d.T, R = (size_t)d.T * d.k;
+    const size_t E = (size_t)d.E;
+    Layout L;
+    size_t o = 0;
+    L.err = o; o += 256;
+    L.tile = o; o += al256((E + 2) * 4);
+    L.hist = o; o += al256((size_t)permute_num_chunks((int64_t)R) * E * 4);
+    L.idx = o; o += al256(R * 4);
+    L.w = o; o += al256(R * 4);
+    L.counts = o; o += al256(E * 4);
+    L.offsets = o; o += al256((E + 1) * 4);
+    L.src = o; o += al256(R * 4);
+    L.inv = o; o += al256(R * 4);
+    L.h = o; o += al256(R * (size_t)d.F * 2);
+    L.hs = o; o += al256(T * (size_t)d.F_shared * 2);
+    L.slot = o; o += al256(((size_t)d.k + (d.F_shared > 0 ? 1 : 0)) * T * (size_t)d.H * 4);
+    L.total = o;
+    return L;
+}
+
+// ----------------------------------------------------------- validation --
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status check_dims(const moe_dims* d)
+{
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->T < 0 || d->H <= 0 || d->F <= 0 || d->E <= 0 || d->k <= 0 || d->F_shared < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (d->k > d->E) return MOE_ERR_INVALID_ARG;
+    if (d->k > 8 || d->E > 256) return MOE_ERR_UNSUPPORTED;
+    if (d->H % 64 || d->F % 64 || d->F_shared % 64) return MOE_ERR_UNSUPPORTED;
+    if (d->T * (int64_t)d->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)d->E * d->H >= ((int64_t)1 << 31) || (int64_t)d->E * d->F >= ((int64_t)1 << 31))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
+
+moe_status check_ws(const moe_dims& d, void* ws, size_t ws_bytes)
+{
+    if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_WORKSPACE;
+    if (ws_bytes < layout_of(d).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status finish(cudaError_t e, void* ws, cudaStream_t s)
+{
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (debug_mode()) {
+        if (ws) return moe_check(ws, (moe_stream_t)s);
+        if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}
+
+#define MOE_TRY(expr)                                  \
+    do {                                               \
+        cudaError_t e_ = (expr);                       \
+        if (e_ != cudaSuccess) return MOE_ERR_CUDA;    \
+    } while (0)
+
+#define MOE_TRY_STATUS(expr)                           \
+    do {                                               \
+        moe_status s_ = (expr);                        \
+        if (s_ != MOE_OK) return s_;                   \
+    } while (0)
+
+unsigned char* bytes(void* p) { return static_cast<unsigned char*>(p); }
+
+// The two grouped GEMMs of one expert set (routed or shared).
+moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, int32_t k,
+                            const uint16_t* x, const int32_t* src_row, const int32_t* tile_start,
+                            const int32_t* offsets, const uint16_t* W1, const uint16_t* W3,
+                            const uint16_t* W2, const float* topk_w, float* slot, uint16_t* h,
+                            uint32_t* err, int sms, cudaStream_t s, moe_event_t ev_mid)
+{
+    if (M == 0) {
+        if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
+        return MOE_OK;
+    }
+    CUtensorMap mx, m1, m3, mh, m2;
+    if (!make_map_2d(&mx, x, (uint64_t)d.H, (uint64_t)d.T, 1) ||
+        !make_map_2d(&m1, W1, (uint64_t)F, (uint64_t)G * d.H, 64) ||
+        !make_map_2d(&m3, W3, (uint64_t)F, (uint64_t)G * d.H, 64) ||
+        !make_map_2d(&mh, h, (uint64_t)F, (uint64_t)M, 128) ||
+        !make_map_2d(&m2, W2, (uint64_t)d.H, (uint64_t)G * F, 64))
+        return MOE_ERR_CUDA;
+    GemmArgs a{};
+    a.M = M;
+    a.G = G;
+    a.k = k;
+    a.T = d.T;
+    a.tile_start = tile_start;
+    a.offsets = offsets;
+    a.src_row = src_row;
+    a.err = err;
+    // GEMM0 + SwiGLU: [rows, H] x [H, F] (W1 and W3) -> h [rows, F]
+    a.N = F;
+    a.K = d.H;
+    a.h_out = reinterpret_cast<__nv_bfloat16*>(h);
+    MOE_TRY(launch_grouped_gemm(kGemm0SwiGLU, mx, m1, m3, a, sms, s));
+    if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
+    // GEMM1 + weighted scatter: h [rows, F] x W2 [F, H] -> slot[rank][token]
+    a.N = d.H;
+    a.K = F;
+    a.h_out = nullptr;
+    a.topk_w = topk_w;
+    a.slot = slot;
+    MOE_TRY(launch_grouped_gemm(kGemm1Scatter, mh, m2, m2, a, sms, s));
+    return MOE_OK;
+}
+
+void record(moe_event_t ev, cudaStream_t s)
+{
+    if (ev) cudaEventRecord((cudaEvent_t)ev, s);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_version(void) { return kVersion; }
+
+const char* moe_status_string(int status)
+{
+    switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG: invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: shape not supported";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace missing, too small or misaligned";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait ran out";
+    case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS: a device index check failed";
+    default: return "unknown moe_status";
+    }
+}
+
+size_t moe_workspace_size(const moe_dims* dims)
+{
+    if (check_dims(dims) != MOE_OK) return 0;
+    return layout_of(*dims).total;
+}
+
+moe_status moe_check(void* ws, moe_stream_t stream)
+{
+    if (!ws) return MOE_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t word = 0;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(&word, ws, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word != 0 && cudaMemset(ws, 0, sizeof word) != cudaSuccess) return MOE_ERR_CUDA;
+    if (word & MOE_DEV_ERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+    if (word & MOE_DEV_ERR_BAD_EXPERT) return MOE_ERR_INVALID_ARG;
+    if (word & MOE_DEV_ERR_BOUNDS) return MOE_ERR_DEVICE_BOUNDS;
+    return MOE_OK;
+}
+
+moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg, const float* bias,
+                     int32_t* topk_idx, float* topk_w, moe_stream_t stream)
+{
+    MOE_TRY_STATUS(check_dims(dims));
+    if (dims->T == 0) return MOE_OK;
+    if (!x || !Wg || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(Wg)) return MOE_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    RouteArgs a{x, Wg, bias, topk_idx, topk_w, dims->T, dims->H, dims->E, dims->k};
+    return finish(launch_route(a, sms, s), nullptr, s);
+}
+
+moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* counts,
+                       int32_t* offsets, int32_t* src_row, int32_t* inv_pos, const moe_bf16* x,
+                       moe_bf16* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream)
+{
+    MOE_TRY_STATUS(check_dims(dims));
+    MOE_TRY_STATUS(check_ws(*dims, ws, ws_bytes));
+    if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+    const int64_t R = dims->T * dims->k;
+    if (R > 0 && (!topk_idx || !src_row || !inv_pos)) return MOE_ERR_INVALID_ARG;
+    if (x_perm && (!x || !aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const Layout L = layout_of(*dims);
+    uint32_t* err = reinterpret_cast<uint32_t*>(bytes(ws) + L.err);
+    PermuteArgs a{topk_idx, counts, offsets, src_row, inv_pos,
+                  reinterpret_cast<int32_t*>(bytes(ws) + L.tile),
+                  reinterpret_cast<int32_t*>(bytes(ws) + L.hist), err, R, dims->E};
+    MOE_TRY(launch_permute(a, s));
+    if (x_perm)
+        MOE_TRY(launch_gather_rows(x, src_row, offsets + dims->E, x_perm, R, dims->T, dims->H,
+                                   dims->k, err, sms, s));
+    return finish(cudaSuccess, ws, s);
+}
+
+moe_status moe_expert_ffn(const moe_dims* dims, const moe_bf16* x, const int32_t* src_row,
+                          const int32_t* offsets, const moe_bf16* W1, const moe_bf16* W3,
+                          const moe_bf16* W2, const float* topk_w, float* slot, void* ws,
+                          size_t ws_bytes, moe_stream_t stream)
+{
+    MOE_TRY_STATUS(check_dims(dims));
+    MOE_TRY_STATUS(check_ws(*dims, ws, ws_bytes));
+    if (dims->T == 0) return MOE_OK;
+    if (!x || !W1 || !W3 || !W2 || !slot) return MOE_ERR_INVALID_ARG;
+    if (!offsets && dims->E != 1) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(slot))
+        return MOE_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const Layout L = layout_of(*dims);
+    uint32_t* err = reinterpret_cast<uint32_t*>(bytes(ws) + L.err);
+    int32_t* tile = nullptr;
+    if (offsets) {
+        tile = reinterpret_cast<int32_t*>(bytes(ws) + L.tile);
+        MOE_TRY(launch_tile_table(offsets, dims->E, tile, s));
+    }
+    const int32_t R = (int32_t)(dims->T * dims->k);
+    MOE_TRY_STATUS(run_expert_gemms(*dims, R, dims->F, dims->E, dims->k, x, src_row, tile, offsets,
+                                    W1, W3, W2, topk_w, slot,
+                                    reinterpret_cast<uint16_t*>(bytes(ws) + L.h), err, sms, s,
+                                    nullptr));
+    return finish(cudaSuccess, ws, s);
+}
+
+moe_status moe_combine(const moe_dims* dims, const float* slot, int32_t n_slots, moe_bf16* out,
+                       moe_stream_t stream)
+{
+    MOE_TRY_STATUS(check_dims(dims));
+    if (dims->T == 0) return MOE_OK;
+    if (!slot || !out || n_slots < 1 || n_slots > 9) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(slot) || !aligned16(out)) return MOE_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    return finish(launch_combine(slot, n_slots, out, dims->T, dims->H, sms, s), nullptr, s);
+}
+
+moe_status moe_layer_forward(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg,
+                             const float* bias, const moe_bf16* W1, const moe_bf16* W3,
+                             const moe_bf16* W2, const moe_bf16* W1s, const moe_bf16* W3s,
+                             const moe_bf16* W2s, moe_bf16* out, const moe_routing_out* routing,
+                             void* ws, size_t ws_bytes, const moe_stage_events* events,
+                             moe_stream_t stream)
+{
+    MOE_TRY_STATUS(check_dims(dims));
+    MOE_TRY_STATUS(check_ws(*dims, ws, ws_bytes));
+    const moe_dims& d = *dims;
+    if (d.T == 0) return MOE_OK;
+    if (!x || !Wg || !W1 || !W3 || !W2 || !out) return MOE_ERR_INVALID_ARG;
+    if (d.F_shared > 0 && (!W1s || !W3s || !W2s)) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, Wg, W1, W3, W2, out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (d.F_shared > 0 && (!aligned16(W1s) || !aligned16(W3s) || !aligned16(W2s)))
+        return MOE_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const Layout L = layout_of(d);
+    unsigned char* w = bytes(ws);
+    uint32_t* err = reinterpret_cast<uint32_t*>(w + L.err);
+    auto pick_i = [&](int32_t* user, size_t off) { return user ? user : reinterpret_cast<int32_t*>(w + off); };
+    int32_t* idx = pick_i(routing ? routing->topk_idx : nullptr, L.idx);
+    float* tw = (routing && routing->topk_w) ? routing->topk_w : reinterpret_cast<float*>(w + L.w);
+    int32_t* counts = pick_i(routing ? routing->counts : nullptr, L.counts);
+    int32_t* offsets = pick_i(routing ? routing->offsets : nullptr, L.offsets);
+    int32_t* src = pick_i(routing ? routing->src_row : nullptr, L.src);
+    int32_t* inv = pick_i(routing ? routing->inv_pos : nullptr, L.inv);
+    int32_t* tile = reinterpret_cast<int32_t*>(w + L.tile);
+    float* slot = reinterpret_cast<float*>(w + L.slot);
+    const int64_t R = d.T * d.k;
+
+    record(events ? events->before_route : nullptr, s);
+    RouteArgs ra{x, Wg, bias, idx, tw, d.T, d.H, d.E, d.k};
+    MOE_TRY(launch_route(ra, sms, s));
+
+    record(events ? events->before_permute : nullptr, s);
+    PermuteArgs pa{idx, counts, offsets, src, inv, tile, reinterpret_cast<int32_t*>(w + L.hist), err,
+                   R, d.E};
+    MOE_TRY(launch_permute(pa, s));
+
+    record(events ? events->before_gemm0 : nullptr, s);
+    MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)R, d.F, d.E, d.k, x, src, tile, offsets, W1, W3, W2,
+                                    tw, slot, reinterpret_cast<uint16_t*>(w + L.h), err, sms, s,
+                                    events ? events->before_gemm1 : nullptr));
+
+    record(events ? events->before_shared : nullptr, s);
+    if (d.F_shared > 0) {
+        MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)d.T, d.F_shared, 1, 1, x, nullptr, nullptr, nullptr,
+                                        W1s, W3s, W2s, nullptr, slot + (size_t)d.k * d.T * d.H,
+                                        reinterpret_cast<uint16_t*>(w + L.hs), err, sms, s, nullptr));
+    }
+
+    record(events ? events->before_combine : nullptr, s);
+    MOE_TRY(launch_combine(slot, d.k + (d.F_shared > 0 ? 1 : 0), out, d.T, d.H, sms, s));
+    record(events ? events->after_combine : nullptr, s);
+    return finish(cudaSuccess, ws, s);
+}
+
+}  // extern "C"

@@ -1,0 +1,385 @@
+// grouped_gemm.cu -- the two expert GEMMs of the layer on the 5th-generation
+// tensor cores (tcgen05 + TMEM), one persistent warp-specialised kernel
+// template with two epilogues.
+//
+// The COMET page splits the first expert GEMM ("Layer 0") along the token
+// dimension M and the second ("Layer 1") along the hidden dimension N
+// ("COMET's Technical Principles", "Tensor Decomposition"), and runs the GEMM
+// thread blocks on asynchronous TMA loads ("Thread Block Isolation"). Here,
+// on one GPU with every expert local:
+//   GEMM0 + SwiGLU (mode kGemm0SwiGLU): M tiles are 128 dispatched rows of one
+//     expert; the producer warp GATHERS those token rows of x straight from
+//     HBM with TMA gather4 (4 rows per instruction, indices from src_row), so
+//     no permuted copy of x is ever written. B is [W1 | W3] for one 128-wide
+//     slice of F: one 128x256 MMA tile gives both x W1 and x W3, and the
+//     epilogue writes h = silu(x W1) * (x W3) in bf16.
+//   GEMM1 + weighted scatter (mode kGemm1Scatter): A = h rows (plain TMA tile),
+//     B = W2 for one 256-wide slice of H (the N split). The epilogue scales
+//     each row by its gate weight and writes it to slot[rank][token] (f32):
+//     every slot is written exactly once, so the later combine is a fixed
+//     rank-order sum with no float atomics.
+//
+// Kernel shape: one CTA per SM (192 threads, ~197 KB of shared memory),
+// persistent over a static schedule of (expert, N tile, M tile) work items
+// read from the device tile table (no host sync). Roles:
+//   warp 0      TMA producer: 4-stage ring of {A 128x64, B 64x256} bf16 tiles,
+//               128-byte swizzle, one mbarrier pair per stage.
+//   warp 1      TMEM allocator (512 columns) and MMA issuer (one thread):
+//               tcgen05.mma.cta_group::1.kind::f16, M=128 N=256 K=16, f32
+//               accumulators in TMEM, double-buffered (2 x 256 columns) so the
+//               epilogue of one tile overlaps the main loop of the next.
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time.
+// Every wait is bounded (ptx.cuh); on a timeout the CTA drains what it
+// issued, frees its TMEM and exits with the error recorded.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = kTileM;   // 128
+constexpr int BN = 256;      // MMA N (GEMM0: 128 of W1 + 128 of W3)
+constexpr int BK = 64;       // 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int B_CHUNK_BYTES = BK * 128;      // one 64-column slice of B: 64 k-rows x 128 B
+constexpr int NUM_THREADS = 192;
+constexpr int MAX_GROUPS = 257;
+constexpr int TMEM_COLS = 512;
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+
+struct SmemTail {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+    int tile_start[MAX_GROUPS + 1];
+    int offsets[MAX_GROUPS + 1];
+};
+
+constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(SmemTail);
+
+struct Work {
+    int g, row0, rows, n_tile;
+};
+
+// Work item w of the static schedule: expert-major, then N tile, then M tile.
+__device__ __forceinline__ Work decode_work(int w, int n_tiles, const int* ts, const int* offs, int G)
+{
+    int lo = 0, hi = G;   // ts[lo]*n <= w < ts[hi]*n
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (ts[mid] * n_tiles <= w) lo = mid; else hi = mid;
+    }
+    Work r;
+    r.g = lo;
+    const int mt = ts[lo + 1] - ts[lo];
+    const int wl = w - ts[lo] * n_tiles;
+    r.n_tile = wl / mt;
+    const int ml = wl - r.n_tile * mt;
+    r.row0 = offs[lo] + ml * BM;
+    r.rows = min(BM, offs[lo + 1] - r.row0);
+    return r;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const GemmArgs args)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t tiles_addr = (raw_addr + 1023u) & ~1023u;
+    unsigned char* tiles = smem_raw + (tiles_addr - raw_addr);
+    SmemTail* st = reinterpret_cast<SmemTail*>(tiles + (size_t)STAGES * STAGE_BYTES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = args.G;
+
+    // ---- set-up
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&st->full[s]), 1);
+            mbar_init(smem_u32(&st->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&st->tfull[a]), 1);
+            mbar_init(smem_u32(&st->tempty[a]), 4);
+        }
+        mbar_init(smem_u32(&st->drain), 1);
+        st->abort = 0;
+        fence_barrier_init();
+    }
+    if (args.tile_start == nullptr) {
+        if (threadIdx.x == 0) {
+            st->tile_start[0] = 0;
+            st->tile_start[1] = (args.M + BM - 1) / BM;
+            st->offsets[0] = 0;
+            st->offsets[1] = args.M;
+        }
+    } else {
+        for (int i = threadIdx.x; i <= G; i += blockDim.x) {
+            st->tile_start[i] = args.tile_start[i];
+            st->offsets[i] = args.offsets[i];
+        }
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB0);
+        if (MODE == kGemm0SwiGLU) tma_prefetch_desc(&tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&st->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    const uint32_t tmem_base = st->tmem_base;
+    const int n_out = (MODE == kGemm0SwiGLU) ? BN / 2 : BN;   // output columns per tile
+    const int n_tiles = (args.N + n_out - 1) / n_out;
+    const int total = st->tile_start[G] * n_tiles;
+    const int k_blocks = args.K / BK;
+    volatile int* abort = &st->abort;
+
+    if (warp == 0) {
+        // ============================ TMA producer ============================
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            const Work wk = decode_work(w, n_tiles, st->tile_start, st->offsets, G);
+            int tok[4] = {0, 0, 0, 0};
+            if (MODE == kGemm0SwiGLU) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int p = wk.row0 + min(4 * lane + r, wk.rows - 1);
+                    const int f = args.src_row ? args.src_row[p] : p;
+                    int t = f / args.k;
+                    if (f < 0 || t >= args.T) {
+                        report_error(args.err, MOE_DEV_ERR_BOUNDS);
+                        t = 0;
+                    }
+                    tok[r] = t;
+                }
+            }
+            const int b_row = wk.g * args.K;
+            for (int kb = 0; kb < k_blocks; ++kb) {
+                // every lane waits; the outcome is made warp-uniform
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(smem_u32(&st->empty[stage]), phase ^ 1u, abort, args.err))) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t full = smem_u32(&st->full[stage]);
+                const uint32_t a_dst = tiles_addr + stage * STAGE_BYTES;
+                const uint32_t b_dst = a_dst + A_BYTES;
+                if (lane == 0) mbar_arrive_expect_tx(full, STAGE_BYTES);
+                __syncwarp();
+                if (MODE == kGemm0SwiGLU) {
+                    tma_gather4(a_dst + lane * 512, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], full);
+                    if (lane == 0) {
+                        const int n0 = wk.n_tile * (BN / 2);
+                        tma_load_2d(b_dst + 0 * B_CHUNK_BYTES, &tmB0, n0, b_row + kb * BK, full);
+                        tma_load_2d(b_dst + 1 * B_CHUNK_BYTES, &tmB0, n0 + 64, b_row + kb * BK, full);
+                        tma_load_2d(b_dst + 2 * B_CHUNK_BYTES, &tmB1, n0, b_row + kb * BK, full);
+                        tma_load_2d(b_dst + 3 * B_CHUNK_BYTES, &tmB1, n0 + 64, b_row + kb * BK, full);
+                    }
+                } else {
+                    if (lane == 0) {
+                        const int n0 = wk.n_tile * BN;
+                        tma_load_2d(a_dst, &tmA, kb * BK, wk.row0, full);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            tma_load_2d(b_dst + j * B_CHUNK_BYTES, &tmB0, n0 + 64 * j, b_row + kb * BK,
+                                        full);
+                    }
+                }
+                ++issued;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok && lane == 0) {
+            // drain: wait (bounded) for the loads still in flight
+            int s = stage;
+            uint32_t ph = phase;
+            for (int i = 0; i < min(issued, STAGES); ++i) {
+                if (s == 0) { s = STAGES - 1; ph ^= 1u; } else { --s; }
+                mbar_wait_drain(smem_u32(&st->full[s]), ph);
+            }
+        }
+    } else if (warp == 1) {
+        // ============================ MMA issuer ==============================
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true;
+            bool any = false;
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                if (!mbar_wait(smem_u32(&st->tempty[acc]), acc_phase ^ 1u, abort, args.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * BN;
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!mbar_wait(smem_u32(&st->full[stage]), phase, abort, args.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_base = tiles_addr + stage * STAGE_BYTES;
+                    const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                        const uint64_t bd = smem_desc_sw128(b_base + kk * 16 * 128, B_CHUNK_BYTES, 1024);
+                        tc_mma_f16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    any = true;
+                    tc_commit(smem_u32(&st->empty[stage]));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit(smem_u32(&st->tfull[acc]));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            if (!ok && any) {
+                // drain: every MMA issued so far must finish before TMEM is freed
+                tc_commit(smem_u32(&st->drain));
+                mbar_wait_drain(smem_u32(&st->drain), 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ============================== epilogue ==============================
+        const int ew = warp & 3;               // TMEM lane quarter this warp may access
+        const int r = ew * 32 + lane;          // row of the tile
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+            const Work wk = decode_work(w, n_tiles, st->tile_start, st->offsets, G);
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&st->tfull[acc]), acc_phase, abort, args.err)))
+                break;
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + ((uint32_t)(ew * 32) << 16) + acc * BN;
+            const bool valid = r < wk.rows;
+            const int p = wk.row0 + r;
+            if (MODE == kGemm0SwiGLU) {
+                const int n0 = wk.n_tile * (BN / 2);
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 32) {
+                    uint32_t va[32], vb[32];
+                    tmem_ld_32x32b_x32(t_row + c, va);
+                    tmem_ld_32x32b_x32(t_row + BN / 2 + c, vb);
+                    tc_wait_ld();
+                    if (valid && n0 + c < args.N) {
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float a0 = __uint_as_float(va[2 * i]);
+                            const float a1 = __uint_as_float(va[2 * i + 1]);
+                            const float b0 = __uint_as_float(vb[2 * i]);
+                            const float b1 = __uint_as_float(vb[2 * i + 1]);
+                            const float g0 = a0 / (1.0f + __expf(-a0)) * b0;
+                            const float g1 = a1 / (1.0f + __expf(-a1)) * b1;
+                            __nv_bfloat162 hv = __floats2bfloat162_rn(g0, g1);
+                            packed[i] = *reinterpret_cast<uint32_t*>(&hv);
+                        }
+                        uint4* dst = reinterpret_cast<uint4*>(args.h_out + (int64_t)p * args.N + n0 + c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
+                                                packed[4 * i + 3]);
+                    }
+                }
+            } else {
+                const int n0 = wk.n_tile * BN;
+                int64_t t = 0;
+                int j = 0;
+                float wt = 1.0f;
+                bool ok_row = valid;
+                if (valid) {
+                    const int f = args.src_row ? args.src_row[p] : p;
+                    t = f / args.k;
+                    j = f - (int)t * args.k;
+                    if (f < 0 || t >= args.T) {
+                        report_error(args.err, MOE_DEV_ERR_BOUNDS);
+                        ok_row = false;
+                    } else if (args.topk_w) {
+                        wt = args.topk_w[f];
+                    }
+                }
+                float* dst_row = args.slot + ((int64_t)j * args.T + t) * args.N + n0;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t v[32];
+                    tmem_ld_32x32b_x32(t_row + c, v);
+                    tc_wait_ld();
+                    if (ok_row && n0 + c < args.N) {
+                        float4* dst = reinterpret_cast<float4*>(dst_row + c);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            dst[i] = make_float4(wt * __uint_as_float(v[4 * i]),
+                                                 wt * __uint_as_float(v[4 * i + 1]),
+                                                 wt * __uint_as_float(v[4 * i + 2]),
+                                                 wt * __uint_as_float(v[4 * i + 3]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&st->tempty[acc]));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    // ---- teardown: every role is done (or has drained after an abort)
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,
+                                const CUtensorMap& tmB1, const GemmArgs& a, int num_sms,
+                                cudaStream_t s)
+{
+    if (a.M == 0) return cudaSuccess;
+    if (a.G < 1 || a.G > MAX_GROUPS - 1) return cudaErrorInvalidValue;
+    if (a.K % BK != 0) return cudaErrorInvalidValue;
+    cudaError_t err;
+    if (mode == kGemm0SwiGLU) {
+        auto kern = grouped_gemm_kernel<kGemm0SwiGLU>;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (err != cudaSuccess) return err;
+        kern<<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB0, tmB1, a);
+    } else {
+        auto kern = grouped_gemm_kernel<kGemm1Scatter>;
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+        if (err != cudaSuccess) return err;
+        kern<<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB0, tmB1, a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace moe

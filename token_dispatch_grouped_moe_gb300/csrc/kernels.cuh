@@ -1,0 +1,77 @@
+// kernels.cuh -- launchers of the layer's kernels (host side), shared by the
+// kernel files and the C ABI (api.cu). Internal to the library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr int kTileM = 128;   // GEMM M tile (routed rows per tile)
+
+struct RouteArgs {
+    const uint16_t* x;     // [T,H] bf16 bits
+    const uint16_t* Wg;    // [H,E]
+    const float* bias;     // [E] or null
+    int32_t* topk_idx;     // [T,k]
+    float* topk_w;         // [T,k]
+    int64_t T;
+    int32_t H, E, k;
+};
+cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s);
+
+struct PermuteArgs {
+    const int32_t* topk_idx;   // [R]
+    int32_t* counts;           // [E]
+    int32_t* offsets;          // [E+1]
+    int32_t* src_row;          // [R]
+    int32_t* inv_pos;          // [R]
+    int32_t* tile_start;       // [E+1]  (M-tile prefix of the GEMMs)
+    int32_t* hist;             // [num_chunks, E] scratch
+    uint32_t* err;
+    int64_t R;
+    int32_t E;
+};
+int permute_num_chunks(int64_t R);
+cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
+
+// x_perm[p] = x[src_row[p] / k] for p < *r_valid (r_valid = &offsets[E]).
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* src_row, const int32_t* r_valid,
+                               uint16_t* x_perm, int64_t R, int64_t T, int32_t H, int32_t k,
+                               uint32_t* err, int num_sms, cudaStream_t s);
+
+cudaError_t launch_tile_table(const int32_t* offsets, int32_t G, int32_t* tile_start,
+                              cudaStream_t s);
+
+enum GemmMode { kGemm0SwiGLU = 0, kGemm1Scatter = 1 };
+
+struct GemmArgs {
+    int32_t M;                   // rows in dispatched order (R, or T for a dense expert)
+    int32_t N;                   // GEMM0: F (per W1 / W3);  GEMM1: H
+    int32_t K;                   // GEMM0: H;  GEMM1: F
+    int32_t G;                   // groups (experts)
+    int32_t k;                   // experts per token: token = f / k, rank = f % k
+    int64_t T;                   // tokens
+    const int32_t* tile_start;   // [G+1] or null (then G == 1: one group of M rows)
+    const int32_t* offsets;      // [G+1] or null (then G == 1)
+    const int32_t* src_row;      // [M] or null (identity)
+    const float* topk_w;         // GEMM1: [M] by f, or null (weight 1)
+    __nv_bfloat16* h_out;        // GEMM0: [M, N]
+    float* slot;                 // GEMM1: [k, T, N]
+    uint32_t* err;
+};
+
+// tmA: GEMM0 -> x [T,H] (box 64 x 1, gathered); GEMM1 -> h [M,F] (box 64 x 128).
+// tmB0/tmB1: GEMM0 -> W1 / W3 viewed as [G*H, F]; GEMM1 -> W2 viewed as [G*F, H]
+// (tmB1 unused). All boxes 64 wide with 128-byte swizzle.
+cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,
+                                const CUtensorMap& tmB1, const GemmArgs& a, int num_sms,
+                                cudaStream_t s);
+
+cudaError_t launch_combine(const float* slot, int32_t n_slots, uint16_t* out, int64_t T, int32_t H,
+                           int num_sms, cudaStream_t s);
+
+}  // namespace moe

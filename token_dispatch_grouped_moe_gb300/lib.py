@@ -1,0 +1,224 @@
+"""Python binding of the C ABI in ``include/moe.h`` (ctypes).
+
+Argument marshalling only: every step of the layer runs in the CUDA library.
+Tensors are torch CUDA tensors (torch provides device memory and streams);
+their data pointers and the current CUDA stream are passed through. If the
+library has not been built, :func:`load` raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmoe_gb300.so")
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_BOUNDS"}
+
+EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check", "moe_route",
+           "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int64), ("H", ctypes.c_int32), ("F", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("F_shared", ctypes.c_int32)]
+
+
+class StageEvents(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("before_route", "before_permute", "before_gemm0",
+                                               "before_gemm1", "before_shared", "before_combine",
+                                               "after_combine")]
+
+
+class RoutingOut(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("topk_idx", "topk_w", "counts", "offsets", "src_row",
+                                               "inv_pos")]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it is missing: build it first)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: run `python -m token_dispatch_grouped_moe_gb300.build`"
+                           " (the MoE layer has no CPU fallback)")
+    lib = ctypes.CDLL(path)
+    P, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    D = ctypes.POINTER(Dims)
+    lib.moe_version.restype = ctypes.c_int
+    lib.moe_version.argtypes = []
+    lib.moe_status_string.restype = ctypes.c_char_p
+    lib.moe_status_string.argtypes = [ctypes.c_int]
+    lib.moe_workspace_size.restype = sz
+    lib.moe_workspace_size.argtypes = [D]
+    lib.moe_check.restype = ctypes.c_int
+    lib.moe_check.argtypes = [P, P]
+    lib.moe_route.restype = ctypes.c_int
+    lib.moe_route.argtypes = [D, P, P, P, P, P, P]
+    lib.moe_permute.restype = ctypes.c_int
+    lib.moe_permute.argtypes = [D, P, P, P, P, P, P, P, P, sz, P]
+    lib.moe_expert_ffn.restype = ctypes.c_int
+    lib.moe_expert_ffn.argtypes = [D, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.moe_combine.restype = ctypes.c_int
+    lib.moe_combine.argtypes = [D, P, i32, P, P]
+    lib.moe_layer_forward.restype = ctypes.c_int
+    lib.moe_layer_forward.argtypes = [D, P, P, P, P, P, P, P, P, P, P, ctypes.POINTER(RoutingOut), P,
+                                      sz, ctypes.POINTER(StageEvents), P]
+    _lib = lib
+    return lib
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ok(status: int, what: str):
+    if status != MOE_OK:
+        raise MoeError(status, what)
+
+
+def make_dims(T, H, F, E, k, F_shared=0) -> Dims:
+    return Dims(int(T), int(H), int(F), int(E), int(k), int(F_shared))
+
+
+def workspace_size(dims: Dims) -> int:
+    return int(load().moe_workspace_size(ctypes.byref(dims)))
+
+
+def workspace(dims: Dims, device=None) -> torch.Tensor:
+    """A zeroed workspace (uint8) for ``dims``; the zeroed head is the error word."""
+    n = workspace_size(dims)
+    if n == 0:
+        raise MoeError(1, "workspace_size")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def check(ws: torch.Tensor, stream=None) -> int:
+    """Synchronise and return (and clear) the device error status in ``ws``."""
+    return int(load().moe_check(_p(ws), _stream(stream)))
+
+
+def route(dims: Dims, x, Wg, bias=None, topk_idx=None, topk_w=None, stream=None):
+    T, k = dims.T, dims.k
+    dev = x.device
+    topk_idx = topk_idx if topk_idx is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
+    topk_w = topk_w if topk_w is not None else torch.empty(T, k, dtype=torch.float32, device=dev)
+    _ok(load().moe_route(ctypes.byref(dims), _p(x), _p(Wg), _p(bias), _p(topk_idx), _p(topk_w),
+                         _stream(stream)), "moe_route")
+    return topk_idx, topk_w
+
+
+def permute(dims: Dims, topk_idx, ws, x=None, want_x_perm=False, stream=None):
+    R, E = dims.T * dims.k, dims.E
+    dev = topk_idx.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    src_row = torch.empty(R, dtype=torch.int32, device=dev)
+    inv_pos = torch.empty(R, dtype=torch.int32, device=dev)
+    x_perm = torch.empty(R, dims.H, dtype=torch.bfloat16, device=dev) if want_x_perm else None
+    _ok(load().moe_permute(ctypes.byref(dims), _p(topk_idx), _p(counts), _p(offsets), _p(src_row),
+                           _p(inv_pos), _p(x), _p(x_perm), _p(ws), ws.numel(), _stream(stream)),
+        "moe_permute")
+    return counts, offsets, src_row, inv_pos, x_perm
+
+
+def expert_ffn(dims: Dims, x, src_row, offsets, W1, W3, W2, topk_w, ws, slot=None, stream=None):
+    if slot is None:
+        slot = torch.empty(dims.k, dims.T, dims.H, dtype=torch.float32, device=x.device)
+    _ok(load().moe_expert_ffn(ctypes.byref(dims), _p(x), _p(src_row), _p(offsets), _p(W1), _p(W3),
+                              _p(W2), _p(topk_w), _p(slot), _p(ws), ws.numel(), _stream(stream)),
+        "moe_expert_ffn")
+    return slot
+
+
+def combine(dims: Dims, slot, n_slots=None, out=None, stream=None):
+    n_slots = n_slots if n_slots is not None else slot.shape[0]
+    if out is None:
+        out = torch.empty(dims.T, dims.H, dtype=torch.bfloat16, device=slot.device)
+    _ok(load().moe_combine(ctypes.byref(dims), _p(slot), int(n_slots), _p(out), _stream(stream)),
+        "moe_combine")
+    return out
+
+
+@dataclass
+class Routing:
+    topk_idx: torch.Tensor
+    topk_w: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    src_row: torch.Tensor
+    inv_pos: torch.Tensor
+
+
+def routing_buffers(dims: Dims, device) -> Routing:
+    R = dims.T * dims.k
+    i32 = dict(dtype=torch.int32, device=device)
+    return Routing(torch.empty(dims.T, dims.k, **i32),
+                   torch.empty(dims.T, dims.k, dtype=torch.float32, device=device),
+                   torch.empty(dims.E, **i32), torch.empty(dims.E + 1, **i32),
+                   torch.empty(R, **i32), torch.empty(R, **i32))
+
+
+def layer_forward(dims: Dims, x, Wg, W1, W3, W2, ws, bias=None, W1s=None, W3s=None, W2s=None,
+                  out=None, routing: Routing | None = None, events: StageEvents | None = None,
+                  stream=None):
+    if out is None:
+        out = torch.empty(dims.T, dims.H, dtype=torch.bfloat16, device=x.device)
+    r = None
+    if routing is not None:
+        r = RoutingOut(*(ctypes.c_void_p(getattr(routing, n).data_ptr()) for n in
+                         ("topk_idx", "topk_w", "counts", "offsets", "src_row", "inv_pos")))
+    _ok(load().moe_layer_forward(ctypes.byref(dims), _p(x), _p(Wg), _p(bias), _p(W1), _p(W3), _p(W2),
+                                 _p(W1s), _p(W3s), _p(W2s), _p(out),
+                                 ctypes.byref(r) if r is not None else None, _p(ws), ws.numel(),
+                                 ctypes.byref(events) if events is not None else None,
+                                 _stream(stream)), "moe_layer_forward")
+    return out
+
+
+class MoELayer:
+    """Weights and a workspace on one device; ``forward(x)`` runs the layer."""
+
+    def __init__(self, Wg, W1, W3, W2, k, bias=None, W1s=None, W3s=None, W2s=None):
+        self.Wg, self.W1, self.W3, self.W2, self.k, self.bias = Wg, W1, W3, W2, int(k), bias
+        self.W1s, self.W3s, self.W2s = W1s, W3s, W2s
+        self.H, self.E = Wg.shape
+        self.F = W1.shape[2]
+        self.Fs = 0 if W1s is None else W1s.shape[1]
+        self._ws = None
+        self._T = None
+
+    def dims(self, T) -> Dims:
+        return make_dims(T, self.H, self.F, self.E, self.k, self.Fs)
+
+    def workspace(self, T):
+        if self._ws is None or self._T != T:
+            self._ws = workspace(self.dims(T), device=self.Wg.device)
+            self._T = T
+        return self._ws
+
+    def forward(self, x, out=None, routing=None, events=None, stream=None):
+        T = x.shape[0]
+        return layer_forward(self.dims(T), x, self.Wg, self.W1, self.W3, self.W2, self.workspace(T),
+                             self.bias, self.W1s, self.W3s, self.W2s, out=out, routing=routing,
+                             events=events, stream=stream)
