@@ -44,4 +44,7 @@ CONFIGS = {
     "dsk-16k": LayerConfig("dsk-16k", T=16384, H=2048, F=1408, E=64, k=6),
     "dsk-32k": LayerConfig("dsk-32k", T=32768, H=2048, F=1408, E=64, k=6),
     "mixtral-zipf": LayerConfig("mixtral-zipf", T=8192, H=4096, F=14336, E=8, k=2, zipf=True),
+    # Mixtral-shaped with T and F quartered: small enough (0.7 GB of weights)
+    # for multi-pass profiler captures, still larger than L2.
+    "mixtral-prof": LayerConfig("mixtral-prof", T=2048, H=4096, F=3584, E=8, k=2),
 }
