@@ -97,6 +97,28 @@ typedef struct {
     int32_t* inv_pos;
 } moe_routing_out;
 
+/* Library-wide options (moe_set_option / moe_get_option). */
+enum {
+    /* How GEMM0 obtains the routed token rows (its A operand):
+     *   MOE_GEMM0_A_PERMUTED   (default) the dispatch step copies them into
+     *                          dispatch order (x_perm, in the workspace) and
+     *                          GEMM0 loads dense 128-row TMA tiles;
+     *   MOE_GEMM0_A_TMA_GATHER the GEMM0 producer warp gathers them straight
+     *                          from x with TMA gather4, 4 rows per instruction.
+     * Both give bit-identical results. */
+    MOE_OPT_GEMM0_A = 0,
+    MOE_GEMM0_A_PERMUTED = 0,
+    MOE_GEMM0_A_TMA_GATHER = 1
+};
+
+/* Sets a library-wide option for later calls (all devices and threads).
+ * Returns MOE_ERR_INVALID_ARG for an unknown option or value. Do not change
+ * options while another thread is inside a call. */
+moe_status moe_set_option(int option, int value);
+
+/* Current value of an option, or -1 for an unknown option. */
+int moe_get_option(int option);
+
 /* Library version (major*10000 + minor*100 + patch). */
 int moe_version(void);
 

@@ -87,6 +87,17 @@ def test_host_validation_without_launch(L):
                                null) == 1
 
 
+def test_options(L):
+    from token_dispatch_grouped_moe_gb300 import lib
+    assert lib.get_gemm0_a() == lib.GEMM0_A_PERMUTED
+    lib.set_gemm0_a(lib.GEMM0_A_TMA_GATHER)
+    assert lib.get_gemm0_a() == lib.GEMM0_A_TMA_GATHER
+    lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
+    assert L.moe_set_option(0, 7) == 1
+    assert L.moe_set_option(3, 0) == 1
+    assert L.moe_get_option(3) == -1
+
+
 def test_zero_tokens_is_noop_on_host(L):
     """T = 0 returns MOE_OK before touching any pointer or the device."""
     from token_dispatch_grouped_moe_gb300 import lib

@@ -173,6 +173,44 @@ def test_zipf_bias_small(lib, oracle):
     assert counts[0] > counts[-1]
 
 
+GATHER_CASES = ["tiny", "ragged", "f_tail", "h_tail_e64", "shared", "one_token", "e256"]
+
+
+@pytest.fixture
+def tma_gather(lib):
+    """Runs the test with GEMM0 gathering its rows by TMA gather4."""
+    lib.set_gemm0_a(lib.GEMM0_A_TMA_GATHER)
+    yield
+    lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
+
+
+@pytest.mark.parametrize("name", GATHER_CASES)
+def test_small_case_tma_gather(lib, oracle, tma_gather, name):
+    """The same edge cases with the TMA gather4 A path."""
+    T, H, F, E, k, Fs = SMALL_CASES[name]
+    run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=1, tol="elementwise")
+
+
+def test_gather_paths_bit_identical(lib):
+    """Both ways of feeding GEMM0 give bit-identical layer outputs."""
+    T, H, F, E, k, Fs = 900, 384, 320, 16, 4, 192
+    inp = make_inputs(T, H, F, E, Fs=Fs, seed=3)
+    g = {n: v.cuda() for n, v in inp.items()}
+    dims = lib.make_dims(T, H, F, E, k, Fs)
+    ws = lib.workspace(dims)
+    outs = []
+    for mode in (lib.GEMM0_A_PERMUTED, lib.GEMM0_A_TMA_GATHER):
+        lib.set_gemm0_a(mode)
+        try:
+            outs.append(lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws,
+                                          W1s=g["W1s"], W3s=g["W3s"], W2s=g["W2s"]).clone())
+        finally:
+            lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+    assert torch.equal(outs[0], outs[1])
+
+
 def test_deterministic(lib, oracle):
     T, H, F, E, k = 700, 256, 256, 8, 2
     inp = make_inputs(T, H, F, E, seed=5)

@@ -22,6 +22,7 @@ constexpr int kMaxDevices = 64;
 // ------------------------------------------------------------ device info --
 
 std::atomic<int> g_num_sms[kMaxDevices];
+std::atomic<int> g_gemm0_a{MOE_GEMM0_A_PERMUTED};
 
 int num_sms_current()
 {
@@ -87,7 +88,7 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t err, tile, hist, idx, w, counts, offsets, src, inv, h, hs, slot, total;
+    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, total;
 };
 
 Layout layout_of(const moe_dims& d)
@@ -105,6 +106,7 @@ Layout layout_of(const moe_dims& d)
     L.offsets = o; o += al256((E + 1) * 4);
     L.src = o; o += al256(R * 4);
     L.inv = o; o += al256(R * 4);
+    L.xp = o; o += al256(R * (size_t)d.H * 2);
     L.h = o; o += al256(R * (size_t)d.F * 2);
     L.hs = o; o += al256(T * (size_t)d.F_shared * 2);
     L.slot = o; o += al256(((size_t)d.k + (d.F_shared > 0 ? 1 : 0)) * T * (size_t)d.H * 4);
@@ -161,19 +163,24 @@ moe_status finish(cudaError_t e, void* ws, cudaStream_t s)
 
 unsigned char* bytes(void* p) { return static_cast<unsigned char*>(p); }
 
-// The two grouped GEMMs of one expert set (routed or shared).
+// The two grouped GEMMs of one expert set (routed or shared). GEMM0 reads its
+// A rows from x_rows ([M,H], already in dispatch order) when given, else it
+// gathers them from x with TMA gather4.
 moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, int32_t k,
-                            const uint16_t* x, const int32_t* src_row, const int32_t* tile_start,
-                            const int32_t* offsets, const uint16_t* W1, const uint16_t* W3,
-                            const uint16_t* W2, const float* topk_w, float* slot, uint16_t* h,
-                            uint32_t* err, int sms, cudaStream_t s, moe_event_t ev_mid)
+                            const uint16_t* x, const uint16_t* x_rows, const int32_t* src_row,
+                            const int32_t* tile_start, const int32_t* offsets, const uint16_t* W1,
+                            const uint16_t* W3, const uint16_t* W2, const float* topk_w, float* slot,
+                            uint16_t* h, uint32_t* err, int sms, cudaStream_t s, moe_event_t ev_mid)
 {
     if (M == 0) {
         if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
         return MOE_OK;
     }
     CUtensorMap mx, m1, m3, mh, m2;
-    if (!make_map_2d(&mx, x, (uint64_t)d.H, (uint64_t)d.T, 1) ||
+    const bool dense = (x_rows != nullptr);
+    const bool ok_a = dense ? make_map_2d(&mx, x_rows, (uint64_t)d.H, (uint64_t)M, 128)
+                            : make_map_2d(&mx, x, (uint64_t)d.H, (uint64_t)d.T, 1);
+    if (!ok_a ||
         !make_map_2d(&m1, W1, (uint64_t)F, (uint64_t)G * d.H, 64) ||
         !make_map_2d(&m3, W3, (uint64_t)F, (uint64_t)G * d.H, 64) ||
         !make_map_2d(&mh, h, (uint64_t)F, (uint64_t)M, 128) ||
@@ -192,7 +199,7 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
     a.N = F;
     a.K = d.H;
     a.h_out = reinterpret_cast<__nv_bfloat16*>(h);
-    MOE_TRY(launch_grouped_gemm(kGemm0SwiGLU, mx, m1, m3, a, sms, s));
+    MOE_TRY(launch_grouped_gemm(dense ? kGemm0Dense : kGemm0Gather, mx, m1, m3, a, sms, s));
     if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
     // GEMM1 + weighted scatter: h [rows, F] x W2 [F, H] -> slot[rank][token]
     a.N = d.H;
@@ -230,6 +237,20 @@ const char* moe_status_string(int status)
     case MOE_ERR_DEVICE_BOUNDS: return "MOE_ERR_DEVICE_BOUNDS: a device index check failed";
     default: return "unknown moe_status";
     }
+}
+
+moe_status moe_set_option(int option, int value)
+{
+    if (option != MOE_OPT_GEMM0_A) return MOE_ERR_INVALID_ARG;
+    if (value != MOE_GEMM0_A_PERMUTED && value != MOE_GEMM0_A_TMA_GATHER) return MOE_ERR_INVALID_ARG;
+    g_gemm0_a.store(value);
+    return MOE_OK;
+}
+
+int moe_get_option(int option)
+{
+    if (option != MOE_OPT_GEMM0_A) return -1;
+    return g_gemm0_a.load();
 }
 
 size_t moe_workspace_size(const moe_dims* dims)
@@ -314,8 +335,19 @@ moe_status moe_expert_ffn(const moe_dims* dims, const moe_bf16* x, const int32_t
         MOE_TRY(launch_tile_table(offsets, dims->E, tile, s));
     }
     const int32_t R = (int32_t)(dims->T * dims->k);
-    MOE_TRY_STATUS(run_expert_gemms(*dims, R, dims->F, dims->E, dims->k, x, src_row, tile, offsets,
-                                    W1, W3, W2, topk_w, slot,
+    const uint16_t* x_rows = nullptr;
+    if (g_gemm0_a.load() == MOE_GEMM0_A_PERMUTED) {
+        if (!src_row && dims->k == 1) {
+            x_rows = x;   // identity dispatch: x is already in dispatch order
+        } else {
+            uint16_t* xp = reinterpret_cast<uint16_t*>(bytes(ws) + L.xp);
+            MOE_TRY(launch_gather_rows(x, src_row, offsets ? offsets + dims->E : nullptr, xp, R,
+                                       dims->T, dims->H, dims->k, err, sms, s));
+            x_rows = xp;
+        }
+    }
+    MOE_TRY_STATUS(run_expert_gemms(*dims, R, dims->F, dims->E, dims->k, x, x_rows, src_row, tile,
+                                    offsets, W1, W3, W2, topk_w, slot,
                                     reinterpret_cast<uint16_t*>(bytes(ws) + L.h), err, sms, s,
                                     nullptr));
     return finish(cudaSuccess, ws, s);
@@ -378,15 +410,23 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_bf16* x, const moe_
                    R, d.E};
     MOE_TRY(launch_permute(pa, s));
 
+    const bool permuted = (g_gemm0_a.load() == MOE_GEMM0_A_PERMUTED);
+    uint16_t* xp = reinterpret_cast<uint16_t*>(w + L.xp);
+    if (permuted)
+        MOE_TRY(launch_gather_rows(x, src, offsets + d.E, xp, R, d.T, d.H, d.k, err, sms, s));
+
     record(events ? events->before_gemm0 : nullptr, s);
-    MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)R, d.F, d.E, d.k, x, src, tile, offsets, W1, W3, W2,
-                                    tw, slot, reinterpret_cast<uint16_t*>(w + L.h), err, sms, s,
+    MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)R, d.F, d.E, d.k, x, permuted ? xp : nullptr, src,
+                                    tile, offsets, W1, W3, W2, tw, slot,
+                                    reinterpret_cast<uint16_t*>(w + L.h), err, sms, s,
                                     events ? events->before_gemm1 : nullptr));
 
     record(events ? events->before_shared : nullptr, s);
     if (d.F_shared > 0) {
-        MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)d.T, d.F_shared, 1, 1, x, nullptr, nullptr, nullptr,
-                                        W1s, W3s, W2s, nullptr, slot + (size_t)d.k * d.T * d.H,
+        // identity dispatch: every token, in token order, weight 1
+        MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)d.T, d.F_shared, 1, 1, x, permuted ? x : nullptr,
+                                        nullptr, nullptr, nullptr, W1s, W3s, W2s, nullptr,
+                                        slot + (size_t)d.k * d.T * d.H,
                                         reinterpret_cast<uint16_t*>(w + L.hs), err, sms, s, nullptr));
     }
 

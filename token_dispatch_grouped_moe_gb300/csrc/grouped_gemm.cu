@@ -7,12 +7,20 @@
 // ("COMET's Technical Principles", "Tensor Decomposition"), and runs the GEMM
 // thread blocks on asynchronous TMA loads ("Thread Block Isolation"). Here,
 // on one GPU with every expert local:
-//   GEMM0 + SwiGLU (mode kGemm0SwiGLU): M tiles are 128 dispatched rows of one
-//     expert; the producer warp GATHERS those token rows of x straight from
-//     HBM with TMA gather4 (4 rows per instruction, indices from src_row), so
-//     no permuted copy of x is ever written. B is [W1 | W3] for one 128-wide
-//     slice of F: one 128x256 MMA tile gives both x W1 and x W3, and the
-//     epilogue writes h = silu(x W1) * (x W3) in bf16.
+//   GEMM0 + SwiGLU: M tiles are 128 dispatched rows of one expert. Two ways to
+//     fetch those token rows (the A operand):
+//       kGemm0Dense  - one TMA box per stage from x_perm, the token rows
+//                      already gathered into dispatch order by the permute
+//                      step (an HBM-bound copy);
+//       kGemm0Gather - the producer warp gathers the rows of x itself with
+//                      TMA gather4 (4 rows per instruction, indices from
+//                      src_row), so no permuted copy of x is written. On GB300
+//                      32 gather4 per 16 KB stage cannot keep up with the
+//                      tensor cores (measured: ~0.5 vs ~1.7 PFLOP/s for the
+//                      Mixtral-shaped GEMM0), so the dense form is the default.
+//     B is [W1 | W3] for one 128-wide slice of F: one 128x256 MMA tile gives
+//     both x W1 and x W3, and the epilogue writes h = silu(x W1) * (x W3) in
+//     bf16.
 //   GEMM1 + weighted scatter (mode kGemm1Scatter): A = h rows (plain TMA tile),
 //     B = W2 for one 256-wide slice of H (the N split). The epilogue scales
 //     each row by its gate weight and writes it to slot[rank][token] (f32):
@@ -103,6 +111,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     unsigned char* tiles = smem_raw + (tiles_addr - raw_addr);
     SmemTail* st = reinterpret_cast<SmemTail*>(tiles + (size_t)STAGES * STAGE_BYTES);
 
+    constexpr bool IS_GEMM0 = (MODE != kGemm1Scatter);
+    constexpr bool GATHER = (MODE == kGemm0Gather);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = args.G;
@@ -137,7 +147,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB0);
-        if (MODE == kGemm0SwiGLU) tma_prefetch_desc(&tmB1);
+        if (IS_GEMM0) tma_prefetch_desc(&tmB1);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&st->tmem_base), TMEM_COLS);
@@ -148,7 +158,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc_fence_after();
 
     const uint32_t tmem_base = st->tmem_base;
-    const int n_out = (MODE == kGemm0SwiGLU) ? BN / 2 : BN;   // output columns per tile
+    const int n_out = IS_GEMM0 ? BN / 2 : BN;   // output columns per tile
     const int n_tiles = (args.N + n_out - 1) / n_out;
     const int total = st->tile_start[G] * n_tiles;
     const int k_blocks = args.K / BK;
@@ -163,7 +173,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
             const Work wk = decode_work(w, n_tiles, st->tile_start, st->offsets, G);
             int tok[4] = {0, 0, 0, 0};
-            if (MODE == kGemm0SwiGLU) {
+            if (GATHER) {
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
                     const int p = wk.row0 + min(4 * lane + r, wk.rows - 1);
@@ -189,8 +199,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint32_t b_dst = a_dst + A_BYTES;
                 if (lane == 0) mbar_arrive_expect_tx(full, STAGE_BYTES);
                 __syncwarp();
-                if (MODE == kGemm0SwiGLU) {
+                if (GATHER)
                     tma_gather4(a_dst + lane * 512, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], full);
+                else if (lane == 0)
+                    tma_load_2d(a_dst, &tmA, kb * BK, wk.row0, full);
+                if (IS_GEMM0) {
                     if (lane == 0) {
                         const int n0 = wk.n_tile * (BN / 2);
                         tma_load_2d(b_dst + 0 * B_CHUNK_BYTES, &tmB0, n0, b_row + kb * BK, full);
@@ -201,7 +214,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 } else {
                     if (lane == 0) {
                         const int n0 = wk.n_tile * BN;
-                        tma_load_2d(a_dst, &tmA, kb * BK, wk.row0, full);
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             tma_load_2d(b_dst + j * B_CHUNK_BYTES, &tmB0, n0 + 64 * j, b_row + kb * BK,
@@ -280,7 +292,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint32_t t_row = tmem_base + ((uint32_t)(ew * 32) << 16) + acc * BN;
             const bool valid = r < wk.rows;
             const int p = wk.row0 + r;
-            if (MODE == kGemm0SwiGLU) {
+            if (IS_GEMM0) {
                 const int n0 = wk.n_tile * (BN / 2);
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
@@ -367,18 +379,14 @@ cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensor
     if (a.M == 0) return cudaSuccess;
     if (a.G < 1 || a.G > MAX_GROUPS - 1) return cudaErrorInvalidValue;
     if (a.K % BK != 0) return cudaErrorInvalidValue;
-    cudaError_t err;
-    if (mode == kGemm0SwiGLU) {
-        auto kern = grouped_gemm_kernel<kGemm0SwiGLU>;
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-        if (err != cudaSuccess) return err;
-        kern<<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB0, tmB1, a);
-    } else {
-        auto kern = grouped_gemm_kernel<kGemm1Scatter>;
-        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
-        if (err != cudaSuccess) return err;
-        kern<<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB0, tmB1, a);
-    }
+    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const GemmArgs);
+    if (mode == kGemm0Gather) kern = grouped_gemm_kernel<kGemm0Gather>;
+    else if (mode == kGemm0Dense) kern = grouped_gemm_kernel<kGemm0Dense>;
+    else if (mode == kGemm1Scatter) kern = grouped_gemm_kernel<kGemm1Scatter>;
+    else return cudaErrorInvalidValue;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    kern<<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB0, tmB1, a);
     return cudaGetLastError();
 }
 

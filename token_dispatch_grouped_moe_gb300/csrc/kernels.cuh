@@ -38,7 +38,8 @@ struct PermuteArgs {
 int permute_num_chunks(int64_t R);
 cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
 
-// x_perm[p] = x[src_row[p] / k] for p < *r_valid (r_valid = &offsets[E]).
+// x_perm[p] = x[src_row[p] / k] for p < *r_valid (r_valid = &offsets[E]);
+// src_row null = identity, r_valid null = all R rows.
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* src_row, const int32_t* r_valid,
                                uint16_t* x_perm, int64_t R, int64_t T, int32_t H, int32_t k,
                                uint32_t* err, int num_sms, cudaStream_t s);
@@ -46,7 +47,9 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* src_row, const 
 cudaError_t launch_tile_table(const int32_t* offsets, int32_t G, int32_t* tile_start,
                               cudaStream_t s);
 
-enum GemmMode { kGemm0SwiGLU = 0, kGemm1Scatter = 1 };
+// GEMM0 + SwiGLU with A gathered from x by TMA gather4 (kGemm0Gather) or read
+// from the dispatch-ordered copy x_perm (kGemm0Dense); GEMM1 + weighted scatter.
+enum GemmMode { kGemm0Gather = 0, kGemm1Scatter = 1, kGemm0Dense = 2 };
 
 struct GemmArgs {
     int32_t M;                   // rows in dispatched order (R, or T for a dense expert)
@@ -64,7 +67,8 @@ struct GemmArgs {
     uint32_t* err;
 };
 
-// tmA: GEMM0 -> x [T,H] (box 64 x 1, gathered); GEMM1 -> h [M,F] (box 64 x 128).
+// tmA: kGemm0Gather -> x [T,H] (box 64 x 1, gathered); kGemm0Dense -> x_perm
+// [M,H] (box 64 x 128); kGemm1Scatter -> h [M,F] (box 64 x 128).
 // tmB0/tmB1: GEMM0 -> W1 / W3 viewed as [G*H, F]; GEMM1 -> W2 viewed as [G*F, H]
 // (tmB1 unused). All boxes 64 wide with 128-byte swizzle.
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,

@@ -175,7 +175,9 @@ __global__ void __launch_bounds__(kScatterThreads) perm_scatter_kernel(PermuteAr
 }
 
 // x_perm[p] = x[src_row[p] / k] for p < offsets[E] (the valid positions;
-// fewer than R only if some expert ids were out of range).
+// fewer than R only if some expert ids were out of range). src_row null means
+// the identity (f = p); r_valid null means all R rows. One warp per row,
+// 16-byte loads and stores: an HBM-bound copy.
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ src_row,
                                    const int32_t* __restrict__ r_valid, uint16_t* __restrict__ x_perm,
                                    int64_t R, int64_t T, int32_t H, int32_t k, uint32_t* err)
@@ -183,9 +185,9 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int vec_per_row = H / 8;
-    const int64_t n = min((int64_t)*r_valid, R);
+    const int64_t n = r_valid ? min((int64_t)*r_valid, R) : R;
     for (int64_t p = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n; p += warps) {
-        const int64_t t = src_row[p] / k;
+        const int64_t t = (src_row ? (int64_t)src_row[p] : p) / k;
         if (t < 0 || t >= T) {
             if (lane == 0) report_error(err, MOE_DEV_ERR_BOUNDS);
             continue;

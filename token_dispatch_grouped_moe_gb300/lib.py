@@ -21,7 +21,12 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_BOUNDS"}
 
 EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check", "moe_route",
-           "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward"]
+           "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_set_option",
+           "moe_get_option"]
+
+OPT_GEMM0_A = 0
+GEMM0_A_PERMUTED = 0      # dispatch copies token rows to x_perm; GEMM0 loads dense tiles
+GEMM0_A_TMA_GATHER = 1    # GEMM0 producer gathers token rows with TMA gather4
 
 
 class MoeError(RuntimeError):
@@ -66,6 +71,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_status_string.argtypes = [ctypes.c_int]
     lib.moe_workspace_size.restype = sz
     lib.moe_workspace_size.argtypes = [D]
+    lib.moe_set_option.restype = ctypes.c_int
+    lib.moe_set_option.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.moe_get_option.restype = ctypes.c_int
+    lib.moe_get_option.argtypes = [ctypes.c_int]
     lib.moe_check.restype = ctypes.c_int
     lib.moe_check.argtypes = [P, P]
     lib.moe_route.restype = ctypes.c_int
@@ -95,6 +104,15 @@ def _stream(stream=None):
 def _ok(status: int, what: str):
     if status != MOE_OK:
         raise MoeError(status, what)
+
+
+def set_gemm0_a(mode: int) -> None:
+    """Choose how GEMM0 obtains its token rows (GEMM0_A_PERMUTED or GEMM0_A_TMA_GATHER)."""
+    _ok(load().moe_set_option(OPT_GEMM0_A, int(mode)), "moe_set_option")
+
+
+def get_gemm0_a() -> int:
+    return int(load().moe_get_option(OPT_GEMM0_A))
 
 
 def make_dims(T, H, F, E, k, F_shared=0) -> Dims:
