@@ -163,6 +163,30 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* c
                        moe_bf16* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * Dispatch with no workspace: the same results as moe_permute (counts,
+ * offsets, src_row, inv_pos and the optional x_perm, bit for bit), for
+ * callers that cannot provide scratch memory -- a host framework that gives
+ * its plug-ins no allocator or scratch hook, or a service whose device memory
+ * budget is fixed at start-up and which must not allocate while serving.
+ * The pages have no counterpart to this entry point; it is an interface
+ * convenience of this library.
+ * Scratch: a fixed 1 MiB array inside the library, one per GPU, held until
+ * the process exits. Shapes whose per-chunk histogram (ceil(T*k / 2048) * E
+ * ints) exceeds 261632 ints are rejected with MOE_ERR_UNSUPPORTED before any
+ * launch (for example E = 64 allows T*k up to 8,372,224).
+ * The first call on a device looks up the array's device address with that
+ * device current; make it before any stream capture on the device. All calls
+ * on a device share the array, which keeps the last call's contents (nothing
+ * in it needs to start at zero); calls that overlap on the GPU race on it and
+ * must be serialised by the caller. No memory is allocated by this call.
+ * An expert id outside [0, E) is skipped (offsets[E] then ends below T*k);
+ * there is no device error word.
+ */
+moe_status moe_permute_static(const moe_dims* dims, const int32_t* topk_idx, int32_t* counts,
+                              int32_t* offsets, int32_t* src_row, int32_t* inv_pos,
+                              const moe_bf16* x, moe_bf16* x_perm, moe_stream_t stream);
+
+/*
  * Expert FFN over the dispatched groups: for every position p of expert e
  * (offsets[e] <= p < offsets[e+1]) with f = src_row[p], t = f / k, j = f % k:
  *   h[p]      = silu(x[t] W1[e]) * (x[t] W3[e])     (GEMM0 + SwiGLU, h in bf16)

@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 
 EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_set_option",
-           "moe_get_option"]
+           "moe_get_option", "moe_permute_static"]
 
 OPT_GEMM0_A = 0
 GEMM0_A_PERMUTED = 0      # dispatch copies token rows to x_perm; GEMM0 loads dense tiles
@@ -81,6 +81,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_route.argtypes = [D, P, P, P, P, P, P]
     lib.moe_permute.restype = ctypes.c_int
     lib.moe_permute.argtypes = [D, P, P, P, P, P, P, P, P, sz, P]
+    lib.moe_permute_static.restype = ctypes.c_int
+    lib.moe_permute_static.argtypes = [D, P, P, P, P, P, P, P, P]
     lib.moe_expert_ffn.restype = ctypes.c_int
     lib.moe_expert_ffn.argtypes = [D, P, P, P, P, P, P, P, P, P, sz, P]
     lib.moe_combine.restype = ctypes.c_int
@@ -157,6 +159,22 @@ def permute(dims: Dims, topk_idx, ws, x=None, want_x_perm=False, stream=None):
     _ok(load().moe_permute(ctypes.byref(dims), _p(topk_idx), _p(counts), _p(offsets), _p(src_row),
                            _p(inv_pos), _p(x), _p(x_perm), _p(ws), ws.numel(), _stream(stream)),
         "moe_permute")
+    return counts, offsets, src_row, inv_pos, x_perm
+
+
+def permute_static(dims: Dims, topk_idx, x=None, want_x_perm=False, stream=None):
+    """Dispatch without a workspace (scratch is a fixed array inside the
+    library; calls on one device must not overlap on the GPU)."""
+    R, E = dims.T * dims.k, dims.E
+    dev = topk_idx.device
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    src_row = torch.empty(R, dtype=torch.int32, device=dev)
+    inv_pos = torch.empty(R, dtype=torch.int32, device=dev)
+    x_perm = torch.empty(R, dims.H, dtype=torch.bfloat16, device=dev) if want_x_perm else None
+    _ok(load().moe_permute_static(ctypes.byref(dims), _p(topk_idx), _p(counts), _p(offsets),
+                                  _p(src_row), _p(inv_pos), _p(x), _p(x_perm), _stream(stream)),
+        "moe_permute_static")
     return counts, offsets, src_row, inv_pos, x_perm
 
 
