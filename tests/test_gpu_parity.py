@@ -165,6 +165,56 @@ def test_tiny_config(lib, oracle):
     run_case(lib, oracle, c.T, c.H, c.F, c.E, c.k, seed=c.seed, tol="elementwise")
 
 
+# Cases whose fp32 logit depends on the summation order (2^24 + 1 rounds to
+# 2^24): (H, [(h, Wg value)], logit in the canonical order). x = 1 at the h.
+ORDER_CASES = [
+    (64, [(0, 2.0 ** 24), (8, 1.0), (9, -2.0 ** 24)], 1.0),     # chunk 1 is its own lane
+    (256, [(0, 2.0 ** 24), (8, 1.0), (128, -2.0 ** 24)], 1.0),  # stride 16 pairs first
+    (320, [(0, 2.0 ** 24), (256, 1.0), (8, -2.0 ** 24)], 0.0),  # chunk 32 wraps to lane 0
+    (64, [(0, -2.0 ** 24), (1, 1.0), (2, 2.0 ** 24)], 1.0),     # increasing h in a chunk
+    (320, [(0, 2.0 ** 24), (128, -2.0 ** 24), (256, 1.0)], 0.0),  # 32 lanes, not 16
+]
+
+
+@pytest.mark.parametrize("E", [2, 16, 32, 64, 200])
+@pytest.mark.parametrize("case", range(len(ORDER_CASES)))
+def test_route_canonical_order(lib, E, case):
+    """The router's logits follow the canonical order bit for bit: expert 0's
+    logit is 1 or 0 depending on the order, expert 1's is exactly 0.5, every
+    other expert's is -1; the top-2 ids and weights reveal expert 0's value.
+    E spans every expert-block variant of the kernel."""
+    H, placements, want = ORDER_CASES[case]
+    x = torch.zeros(1, H)
+    Wg = torch.zeros(H, E)
+    for h, v in placements:
+        x[0, h] = 1.0
+        Wg[h, 0] = v
+    h0 = placements[0][0]
+    Wg[h0, 1] = 0.5
+    Wg[h0, 2:] = -1.0
+    dims = lib.make_dims(1, H, 64, E, 2)
+    idx, w = lib.route(dims, x.bfloat16().cuda(), Wg.bfloat16().cuda())
+    torch.cuda.synchronize()
+    idx, w = idx.cpu().tolist()[0], w.cpu().double().numpy()[0]
+    assert idx == ([0, 1] if want == 1.0 else [1, 0])
+    assert abs(w[0] - 1.0 / (1.0 + np.exp(-0.5))) < 1e-6
+
+
+def test_route_bias_added_after_sum(lib):
+    """The bias is one fp32 add after the lane reduction: a bias that exactly
+    offsets a logit difference produces a tie, broken to the lower id."""
+    H, E = 128, 4
+    x = torch.zeros(1, H)
+    x[0, 0] = 1.0
+    Wg = torch.zeros(H, E)
+    Wg[0] = torch.tensor([0.25, 0.75, 0.5, -1.0])
+    bias = torch.tensor([0.5, 0.0, 0.0, 0.0])      # expert 0: 0.75, expert 1: 0.75 -> tie
+    dims = lib.make_dims(1, H, 64, E, 2)
+    idx, _ = lib.route(dims, x.bfloat16().cuda(), Wg.bfloat16().cuda(), bias=bias.cuda())
+    torch.cuda.synchronize()
+    assert idx.cpu().tolist()[0] == [0, 1]
+
+
 def test_zipf_bias_small(lib, oracle):
     """Biased (skewed) routing on a Mixtral-like E=8 top-2 layer at small H/F."""
     bias = zipf_bias()
