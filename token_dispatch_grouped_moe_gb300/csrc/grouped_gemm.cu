@@ -313,11 +313,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             __nv_bfloat162 hv = __floats2bfloat162_rn(g0, g1);
                             packed[i] = *reinterpret_cast<uint32_t*>(&hv);
                         }
-                        uint4* dst = reinterpret_cast<uint4*>(args.h_out + (int64_t)p * args.N + n0 + c);
+                        // 64 bytes of this row: two whole-sector stores
+                        __nv_bfloat16* dst = args.h_out + (int64_t)p * args.N + n0 + c;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2],
-                                                packed[4 * i + 3]);
+                        for (int i = 0; i < 2; ++i)
+                            st_global_v8(dst + 16 * i, packed[8 * i], packed[8 * i + 1], packed[8 * i + 2],
+                                         packed[8 * i + 3], packed[8 * i + 4], packed[8 * i + 5],
+                                         packed[8 * i + 6], packed[8 * i + 7]);
                     }
                 }
             } else {
@@ -344,13 +346,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tmem_ld_32x32b_x32(t_row + c, v);
                     tc_wait_ld();
                     if (ok_row && n0 + c < args.N) {
-                        float4* dst = reinterpret_cast<float4*>(dst_row + c);
+                        // 128 bytes of this row: four whole-sector stores
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            dst[i] = make_float4(wt * __uint_as_float(v[4 * i]),
-                                                 wt * __uint_as_float(v[4 * i + 1]),
-                                                 wt * __uint_as_float(v[4 * i + 2]),
-                                                 wt * __uint_as_float(v[4 * i + 3]));
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t o[8];
+#pragma unroll
+                            for (int u = 0; u < 8; ++u)
+                                o[u] = __float_as_uint(wt * __uint_as_float(v[8 * i + u]));
+                            st_global_v8(dst_row + c + 8 * i, o[0], o[1], o[2], o[3], o[4], o[5], o[6],
+                                         o[7]);
+                        }
                     }
                 }
             }

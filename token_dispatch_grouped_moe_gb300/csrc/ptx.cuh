@@ -221,6 +221,17 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&v)
         : "memory");
 }
 
+// 32-byte store of 8 words (a whole L2 sector). The address must be 32-byte
+// aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, uint32_t w0, uint32_t w1, uint32_t w2,
+                                             uint32_t w3, uint32_t w4, uint32_t w5, uint32_t w6,
+                                             uint32_t w7)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(w0),
+                 "r"(w1), "r"(w2), "r"(w3), "r"(w4), "r"(w5), "r"(w6), "r"(w7)
+                 : "memory");
+}
+
 // ------------------------------------------------------- UMMA descriptors --
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
