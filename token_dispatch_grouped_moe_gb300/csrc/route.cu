@@ -276,27 +276,32 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
-template <int CS_, int EW_, int EWG_, int NT_>
+template <int CS_, int EW_, int EWG_, int NT_, bool WF32_, int MINB_>
 struct CShape {
     static constexpr int CS = CS_;                  // CTAs per cluster (canonical lane split)
     static constexpr int EW = EW_;                  // experts per thread
     static constexpr int EWG = EWG_;                // expert subgroups of warps
     static constexpr int NT = NT_;                  // tokens per thread
+    static constexpr bool WF32 = WF32_;             // gate kept as fp32 (else bf16) in smem
+    static constexpr int MINB = MINB_;              // CTAs per SM the registers must allow
     static constexpr int LC = 32 / CS;              // canonical lanes per CTA
     static constexpr int EB = EW * EWG;             // experts held (E padded)
-    static constexpr int Q = EB / 8;                // expert octets
+    static constexpr int VW = WF32 ? 4 : 8;         // experts per 16-byte gate word
+    static constexpr int QV = EB / VW;              // gate words per (step, element, lane)
     static constexpr int TS = kCWarps / EWG;        // token subgroups of warps
     static constexpr int TB = TS * CS * NT;         // tokens per group
-    static constexpr int GATE_STEP_U4 = 8 * Q * LC; // gate uint4 per step
-    static constexpr int X_STEP_U4 = TB * LC;       // x uint4 per step
+    static constexpr int TBO = TB / CS;             // tokens of a group finished by each rank
+    static constexpr int GATE_STEP_U4 = 8 * QV * LC;
+    static constexpr int X_STEP_U4 = TB * LC;
     static constexpr int LOG_LC = LC == 32 ? 5 : LC == 16 ? 4 : LC == 8 ? 3 : 2;
-    static constexpr int LOG_Q = Q == 1 ? 0 : Q == 2 ? 1 : Q == 4 ? 2 : 3;
+    static constexpr int LOG_QV = QV == 1 ? 0 : QV == 2 ? 1 : QV == 4 ? 2 : QV == 8 ? 3 : 4;
+    static_assert((1 << LOG_QV) == QV && (1 << LOG_LC) == LC, "power-of-two shapes");
 
     static size_t smem_bytes(int H, int E)
     {
         const size_t n_steps = (size_t)(H / 8 + 31) / 32;
         return n_steps * GATE_STEP_U4 * 16 + (size_t)kRing * X_STEP_U4 * 16 +
-               (size_t)(CS - 1) * TB * EB * 4 + (size_t)TB * E * 4;
+               (size_t)CS * TBO * EB * 4 + (size_t)TBO * E * 4;
     }
 };
 
@@ -341,8 +346,78 @@ __device__ __forceinline__ void reduced_slots(int r, int& first, int& count, boo
     writer = (r & dup) == 0;
 }
 
+// The gate words of this CTA's canonical lanes, all steps, into shared memory:
+// layout [step m][element i][word q][sub-lane r]; word q holds experts
+// VW*q .. VW*q+VW-1 of hidden row h = 256 m + 8 (r*CS + rank) + i.
 template <class S>
-__global__ void __launch_bounds__(kCThreads, 1) route_cluster_kernel(RouteArgs a)
+__device__ void stage_gate_cluster(uint4* gate, const uint16_t* __restrict__ Wg, int H, int E, int n_steps,
+                                   int rank)
+{
+    const int total = n_steps * S::GATE_STEP_U4;
+    auto coords = [&](int idx, int& h, int& e) {
+        const int rr = idx & (S::LC - 1);
+        const int rest = idx >> S::LOG_LC;
+        const int q = rest & (S::QV - 1);
+        const int i = (rest >> S::LOG_QV) & 7;
+        const int m = rest >> (S::LOG_QV + 3);
+        h = m * 256 + 8 * (rr * S::CS + rank) + i;
+        e = S::VW * q;
+    };
+    if constexpr (!S::WF32) {
+        const bool vec = (E % 8 == 0);
+        for (int idx = threadIdx.x; idx < total; idx += kCThreads) {
+            int h, e;
+            coords(idx, h, e);
+            if (vec) {
+                const bool in = (h < H) && (e + 8 <= E);
+                cp_async_16(smem_u32(gate + idx), in ? Wg + (int64_t)h * E + e : Wg, in ? 16u : 0u);
+            } else {
+                uint32_t w[4] = {0, 0, 0, 0};
+                if (h < H)
+                    for (int u = 0; u < 8 && e + u < E; ++u)
+                        w[u >> 1] |= (uint32_t)Wg[(int64_t)h * E + e + u] << (16 * (u & 1));
+                gate[idx] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    } else {
+        // fp32 words: loads issued in batches of 8 per thread, then widened
+        const bool vec = (E % 4 == 0);
+        constexpr int B = 8;
+        for (int base = threadIdx.x; base < total; base += B * kCThreads) {
+            uint2 raw[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int idx = base + b * kCThreads;
+                raw[b] = make_uint2(0, 0);
+                if (idx < total) {
+                    int h, e;
+                    coords(idx, h, e);
+                    if (h < H) {
+                        const uint16_t* src = Wg + (int64_t)h * E + e;
+                        if (vec && e + 4 <= E) {
+                            raw[b] = __ldg(reinterpret_cast<const uint2*>(src));
+                        } else {
+                            uint32_t w[2] = {0, 0};
+                            for (int u = 0; u < 4 && e + u < E; ++u)
+                                w[u >> 1] |= (uint32_t)src[u] << (16 * (u & 1));
+                            raw[b] = make_uint2(w[0], w[1]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int idx = base + b * kCThreads;
+                if (idx < total)
+                    reinterpret_cast<float4*>(gate)[idx] =
+                        make_float4(bf16_lo(raw[b].x), bf16_hi(raw[b].x), bf16_lo(raw[b].y), bf16_hi(raw[b].y));
+            }
+        }
+    }
+}
+
+template <class S>
+__global__ void __launch_bounds__(kCThreads, S::MINB) route_cluster_kernel(RouteArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     cg::cluster_group cluster = cg::this_cluster();
@@ -359,45 +434,16 @@ __global__ void __launch_bounds__(kCThreads, 1) route_cluster_kernel(RouteArgs a
 
     uint4* gate = reinterpret_cast<uint4*>(smem_raw);
     uint4* ring = gate + (size_t)n_steps * S::GATE_STEP_U4;
-    float* red = reinterpret_cast<float*>(ring + kRing * S::X_STEP_U4);   // (CS-1) x [TB][EB]
-    float* logit_s = red + (S::CS - 1) * S::TB * S::EB;                   // [TB][E]
+    float* red = reinterpret_cast<float*>(ring + kRing * S::X_STEP_U4);   // [CS][TBO][EB]
+    float* logit_s = red + S::CS * S::TBO * S::EB;                       // [TBO][E]
 
     const int64_t n_clusters = gridDim.x / S::CS;
     const int64_t group_stride = n_clusters * S::TB;
     int64_t t0 = (int64_t)(blockIdx.x / S::CS) * S::TB;
     if (t0 >= a.T) return;   // the whole cluster leaves together
 
-    // the gate, this CTA's canonical lanes only, once
-    {
-        const int total = n_steps * S::GATE_STEP_U4;
-        const bool vec = (E % 8 == 0);
-        for (int idx = threadIdx.x; idx < total; idx += kCThreads) {
-            const int rr = idx & (S::LC - 1);
-            const int rest = idx >> S::LOG_LC;
-            const int q = rest & (S::Q - 1);
-            const int i = (rest >> S::LOG_Q) & 7;
-            const int m = rest >> (S::LOG_Q + 3);
-            const int h = m * 256 + 8 * (rr * S::CS + rank) + i;
-            const int e = 8 * q;
-            if (vec) {
-                const bool in = (h < H) && (e + 8 <= E);
-                cp_async_16(smem_u32(gate + idx), in ? a.Wg + (int64_t)h * E + e : a.Wg, in ? 16u : 0u);
-            } else {
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (h < H) {
-                    const uint16_t* src = a.Wg + (int64_t)h * E + e;
-                    uint16_t t[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) t[u] = (e + u < E) ? src[u] : (uint16_t)0;
-                    v.x = t[0] | ((uint32_t)t[1] << 16);
-                    v.y = t[2] | ((uint32_t)t[3] << 16);
-                    v.z = t[4] | ((uint32_t)t[5] << 16);
-                    v.w = t[6] | ((uint32_t)t[7] << 16);
-                }
-                gate[idx] = v;
-            }
-        }
-    }
+    stage_gate_cluster<S>(gate, a.Wg, H, E, n_steps, rank);
+
     // x of one step for the group starting at g0 into ring slot `sl`
     auto stage_x = [&](int sl, int64_t g0, int m) {
 #pragma unroll
@@ -413,7 +459,7 @@ __global__ void __launch_bounds__(kCThreads, 1) route_cluster_kernel(RouteArgs a
         }
     };
     // prefetch cursor, kRing-1 steps ahead (commit groups: prologue 0..kRing-2,
-    // step number s commits s + kRing - 1; the gate is in group 0)
+    // step number s commits s + kRing - 1; the bf16 gate copies are in group 0)
     int64_t pf_t0 = t0;
     int pf_m = 0, pf_slot = 0;
     auto pf_issue = [&]() {
@@ -433,6 +479,7 @@ __global__ void __launch_bounds__(kCThreads, 1) route_cluster_kernel(RouteArgs a
     bool writer;
     reduced_slots<S::EW, S::LC>(r, first, count, writer);
     constexpr int MAXC = S::EW / S::LC > 0 ? S::EW / S::LC : 1;
+    auto tok = [&](int jt) { return (ts * S::CS + slot) * S::NT + jt; };
 
     float acc[S::NT][S::EW];
     int cur_slot = 0;
@@ -450,7 +497,7 @@ __global__ void __launch_bounds__(kCThreads, 1) route_cluster_kernel(RouteArgs a
             __syncthreads();
 
             const uint4* xs = ring + cur_slot * S::X_STEP_U4 + ((ts * S::CS + slot) * S::NT) * S::LC + r;
-            const uint4* gs = gate + (size_t)m * S::GATE_STEP_U4 + (eg * (S::EW / 8)) * S::LC + r;
+            const uint4* gs = gate + (size_t)m * S::GATE_STEP_U4 + (eg * (S::EW / S::VW)) * S::LC + r;
             uint4 xv[S::NT];
 #pragma unroll
             for (int jt = 0; jt < S::NT; ++jt) xv[jt] = xs[jt * S::LC];
@@ -464,128 +511,121 @@ __global__ void __launch_bounds__(kCThreads, 1) route_cluster_kernel(RouteArgs a
                     xf[jt] = (i & 1) ? bf16_hi(word) : bf16_lo(word);
                 }
 #pragma unroll
-                for (int q = 0; q < S::EW / 8; ++q) {
-                    const uint4 w = gs[(i * S::Q + q) * S::LC];
-                    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                for (int q = 0; q < S::EW / S::VW; ++q) {
+                    const uint4 w = gs[(i * S::QV + q) * S::LC];
+                    float wf[S::VW];
+                    if constexpr (S::WF32) {
+                        wf[0] = __uint_as_float(w.x); wf[1] = __uint_as_float(w.y);
+                        wf[2] = __uint_as_float(w.z); wf[3] = __uint_as_float(w.w);
+                    } else {
+                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float wl = bf16_lo(ww[u]);
-                        const float wh = bf16_hi(ww[u]);
-#pragma unroll
-                        for (int jt = 0; jt < S::NT; ++jt) {
-                            acc[jt][8 * q + 2 * u] = fmaf(xf[jt], wl, acc[jt][8 * q + 2 * u]);
-                            acc[jt][8 * q + 2 * u + 1] = fmaf(xf[jt], wh, acc[jt][8 * q + 2 * u + 1]);
+                        for (int u = 0; u < 4; ++u) {
+                            wf[2 * u] = bf16_lo(ww[u]);
+                            wf[2 * u + 1] = bf16_hi(ww[u]);
                         }
                     }
+#pragma unroll
+                    for (int u = 0; u < S::VW; ++u)
+#pragma unroll
+                        for (int jt = 0; jt < S::NT; ++jt)
+                            acc[jt][S::VW * q + u] = fmaf(xf[jt], wf[u], acc[jt][S::VW * q + u]);
                 }
             }
             if (++cur_slot == kRing) cur_slot = 0;
         }
 
         // butterfly levels with stride >= CS, inside the CTA
-        float own[S::NT][MAXC];
 #pragma unroll
-        for (int jt = 0; jt < S::NT; ++jt) {
-            transpose_reduce<S::EW, S::LC / 2>(acc[jt], r);
-#pragma unroll
-            for (int c = 0; c < MAXC; ++c) own[jt][c] = acc[jt][c];
-        }
+        for (int jt = 0; jt < S::NT; ++jt) transpose_reduce<S::EW, S::LC / 2>(acc[jt], r);
         const int e_base = eg * S::EW + first;
-        auto tok = [&](int jt) { return (ts * S::CS + slot) * S::NT + jt; };
 
-        if constexpr (S::CS > 1) {
-            cluster.sync();   // rank 0 is done with the previous group's partial sums
-            if (rank != 0 && writer) {
-                float* dst = cluster.map_shared_rank(red, 0) + (rank - 1) * S::TB * S::EB;
+        // each rank finishes the tokens tt with tt mod CS == rank: every rank
+        // sends it its partial sums (its own included)
+        cluster.sync();   // the owners are done with the previous group's partial sums
+        if (writer) {
 #pragma unroll
-                for (int jt = 0; jt < S::NT; ++jt)
+            for (int jt = 0; jt < S::NT; ++jt) {
+                const int tt = tok(jt);
+                float* dst = (S::CS > 1 ? cluster.map_shared_rank(red, tt % S::CS) : red) +
+                             (rank * S::TBO + tt / S::CS) * S::EB + e_base;
 #pragma unroll
-                    for (int c = 0; c < MAXC; ++c)
-                        if (c < count) dst[tok(jt) * S::EB + e_base + c] = own[jt][c];
+                for (int c = 0; c < MAXC; ++c)
+                    if (c < count) dst[c] = acc[jt][c];
             }
-            cluster.sync();   // every partial sum has arrived at rank 0
         }
-        if (rank == 0) {
-            // butterfly levels with stride < CS across the ranks, then the bias
-            if (writer) {
+        cluster.sync();   // every partial sum has arrived at its owner
+        // butterfly levels with stride < CS across the ranks, then the bias
+        for (int idx = threadIdx.x; idx < S::TBO * E; idx += kCThreads) {
+            const int u = idx / E, e = idx - u * E;
+            float v[S::CS];
 #pragma unroll
-                for (int jt = 0; jt < S::NT; ++jt)
+            for (int rho = 0; rho < S::CS; ++rho) v[rho] = red[(rho * S::TBO + u) * S::EB + e];
 #pragma unroll
-                    for (int c = 0; c < MAXC; ++c) {
-                        const int e = e_base + c;
-                        if (c < count && e < E) {
-                            float v[S::CS];
-                            v[0] = own[jt][c];
+            for (int st = S::CS / 2; st >= 1; st >>= 1) {
+                float nv[S::CS];
 #pragma unroll
-                            for (int rho = 1; rho < S::CS; ++rho)
-                                v[rho] = red[(rho - 1) * S::TB * S::EB + tok(jt) * S::EB + e];
+                for (int rho = 0; rho < S::CS; ++rho) nv[rho] = v[rho] + v[rho ^ st];
 #pragma unroll
-                            for (int st = S::CS / 2; st >= 1; st >>= 1) {
-                                float nv[S::CS];
-#pragma unroll
-                                for (int rho = 0; rho < S::CS; ++rho) nv[rho] = v[rho] + v[rho ^ st];
-#pragma unroll
-                                for (int rho = 0; rho < S::CS; ++rho) v[rho] = nv[rho];
-                            }
-                            float l = v[0];
-                            if (a.bias) l = l + a.bias[e];
-                            logit_s[tok(jt) * E + e] = l;
-                        }
-                    }
+                for (int rho = 0; rho < S::CS; ++rho) v[rho] = nv[rho];
             }
-            __syncthreads();
-            // top-k per token by one warp: each lane scans experts e = lane, lane+32;
-            // a warp argmax (larger value, ties to the lower id) picks each rank.
-            for (int tt = warp; tt < S::TB; tt += kCWarps) {
-                const int64_t t = t0 + tt;
-                if (t >= a.T) break;
-                const float* l = logit_s + tt * E;
-                uint32_t taken = 0;
-                int sel_e[8];
-                float sel_l[8];
+            float l = v[0];
+            if (a.bias) l = l + a.bias[e];
+            logit_s[idx] = l;
+        }
+        __syncthreads();
+        // top-k of this rank's tokens, one warp per token: each lane scans experts
+        // e = lane, lane+32; a warp argmax (larger value, ties to the lower id).
+        for (int u = warp; u < S::TBO; u += kCWarps) {
+            const int64_t t = t0 + (int64_t)u * S::CS + rank;
+            if (t >= a.T) break;
+            const float* l = logit_s + u * E;
+            uint32_t taken = 0;
+            int sel_e[8];
+            float sel_l[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= k) break;
+                float bv = 0.0f;
+                int be = -1;
+                for (int uu = 0; lane + 32 * uu < E; ++uu) {
+                    if (taken & (1u << uu)) continue;
+                    const float v = l[lane + 32 * uu];
+                    if (be < 0 || v > bv) { bv = v; be = lane + 32 * uu; }
+                }
+#pragma unroll
+                for (int st = 16; st >= 1; st >>= 1) {
+                    const float ov = __shfl_xor_sync(kFull, bv, st);
+                    const int oe = __shfl_xor_sync(kFull, be, st);
+                    const bool better = (oe >= 0) && (be < 0 || ov > bv || (ov == bv && oe < be));
+                    if (better) { bv = ov; be = oe; }
+                }
+                if ((be & 31) == lane) taken |= 1u << (be >> 5);
+                sel_e[j] = be;
+                sel_l[j] = bv;
+            }
+            if (lane == 0) {
+                const float mx = sel_l[0];
+                float ex[8];
+                float den = 0.0f;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     if (j >= k) break;
-                    float bv = 0.0f;
-                    int be = -1;
-                    for (int u = 0; lane + 32 * u < E; ++u) {
-                        if (taken & (1u << u)) continue;
-                        const float v = l[lane + 32 * u];
-                        if (be < 0 || v > bv) { bv = v; be = lane + 32 * u; }
-                    }
-#pragma unroll
-                    for (int st = 16; st >= 1; st >>= 1) {
-                        const float ov = __shfl_xor_sync(kFull, bv, st);
-                        const int oe = __shfl_xor_sync(kFull, be, st);
-                        const bool better = (oe >= 0) && (be < 0 || ov > bv || (ov == bv && oe < be));
-                        if (better) { bv = ov; be = oe; }
-                    }
-                    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-                    sel_e[j] = be;
-                    sel_l[j] = bv;
+                    ex[j] = expf(sel_l[j] - mx);
+                    den = den + ex[j];
                 }
-                if (lane == 0) {
-                    const float mx = sel_l[0];
-                    float ex[8];
-                    float den = 0.0f;
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (j >= k) break;
-                        ex[j] = expf(sel_l[j] - mx);
-                        den = den + ex[j];
-                    }
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        if (j >= k) break;
-                        a.topk_idx[t * k + j] = sel_e[j];
-                        a.topk_w[t * k + j] = ex[j] / den;
-                    }
+                for (int j = 0; j < 8; ++j) {
+                    if (j >= k) break;
+                    a.topk_idx[t * k + j] = sel_e[j];
+                    a.topk_w[t * k + j] = ex[j] / den;
                 }
             }
         }
         t0 += group_stride;
     }
     cp_async_wait<0>();   // nothing in flight at exit
+    if (S::CS > 1) cluster.sync();   // no rank leaves while another may still read its smem
 }
 
 template <class S>
@@ -596,11 +636,7 @@ cudaError_t launch_cluster(const RouteArgs& a, int num_sms, cudaStream_t s)
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     const int64_t groups = (a.T + S::TB - 1) / S::TB;
-    int64_t clusters = num_sms / S::CS;
-    if (clusters > groups) clusters = groups;
-    if (clusters < 1) clusters = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(clusters * S::CS));
     cfg.blockDim = dim3(kCThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -611,32 +647,36 @@ cudaError_t launch_cluster(const RouteArgs& a, int num_sms, cudaStream_t s)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (S::CS > 1) {
-        int max_clusters = 0;
-        if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) == cudaSuccess && max_clusters > 0 &&
-            clusters > max_clusters) {
-            clusters = max_clusters;
-            cfg.gridDim = dim3((unsigned)(clusters * S::CS));
-        }
-    }
+    int64_t clusters = (int64_t)num_sms * S::MINB / S::CS;
+    cfg.gridDim = dim3((unsigned)(clusters * S::CS));
+    int max_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) == cudaSuccess && max_clusters > 0)
+        clusters = max_clusters;
+    if (clusters > groups) clusters = groups;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3((unsigned)(clusters * S::CS));
     err = cudaLaunchKernelEx(&cfg, kern, a);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
-// The smallest cluster whose per-CTA share of the gate fits; -1 if none.
-template <int EW, int EWG, int NT>
+// The first cluster shape (in the order given) whose shared memory fits.
+template <int EW, int EWG, int NT, int MINB, int CS0>
 cudaError_t launch_cluster_any(const RouteArgs& a, int num_sms, cudaStream_t s, bool& launched)
 {
     launched = true;
-    if (CShape<1, EW, EWG, NT>::smem_bytes(a.H, a.E) <= kSmemBudget)
-        return launch_cluster<CShape<1, EW, EWG, NT>>(a, num_sms, s);
-    if (CShape<2, EW, EWG, NT>::smem_bytes(a.H, a.E) <= kSmemBudget)
-        return launch_cluster<CShape<2, EW, EWG, NT>>(a, num_sms, s);
-    if (CShape<4, EW, EWG, NT>::smem_bytes(a.H, a.E) <= kSmemBudget)
-        return launch_cluster<CShape<4, EW, EWG, NT>>(a, num_sms, s);
-    if (CShape<8, EW, EWG, NT>::smem_bytes(a.H, a.E) <= kSmemBudget)
-        return launch_cluster<CShape<8, EW, EWG, NT>>(a, num_sms, s);
+#define MOE_TRY_SHAPE(CS, F32)                                                                 \
+    if ((CS) >= CS0 && CShape<CS, EW, EWG, NT, F32, MINB>::smem_bytes(a.H, a.E) <= kSmemBudget) \
+        return launch_cluster<CShape<CS, EW, EWG, NT, F32, MINB>>(a, num_sms, s);
+    // clusters of 8 are placed on fewer SMs (15 clusters, 120 SMs, measured),
+    // so a bf16 gate in a cluster of <= 4 beats an fp32 gate in a cluster of 8
+    MOE_TRY_SHAPE(2, true)
+    MOE_TRY_SHAPE(4, true)
+    MOE_TRY_SHAPE(2, false)
+    MOE_TRY_SHAPE(4, false)
+    MOE_TRY_SHAPE(8, true)
+    MOE_TRY_SHAPE(8, false)
+#undef MOE_TRY_SHAPE
     launched = false;
     return cudaSuccess;
 }
@@ -648,16 +688,16 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s)
     if (a.T == 0) return cudaSuccess;
     bool launched = false;
     cudaError_t err = cudaSuccess;
-    // E <= 8: the whole gate fits one CTA and route_kernel measured faster
-    // (38.8 vs 42.8 us for 8192 x 4096, E = 8); the cluster kernel wins above.
+    // E <= 8: the whole gate fits one CTA; route_kernel measured faster there
+    // (38.8 vs 44.0 us for 8192 x 4096, E = 8).
     if (a.E <= 8)
         launched = false;
     else if (a.E <= 16)
-        err = launch_cluster_any<16, 1, 2>(a, num_sms, s, launched);
+        err = launch_cluster_any<16, 1, 2, 1, 2>(a, num_sms, s, launched);
     else if (a.E <= 32)
-        err = launch_cluster_any<16, 2, 4>(a, num_sms, s, launched);
+        err = launch_cluster_any<16, 2, 4, 1, 2>(a, num_sms, s, launched);
     else if (a.E <= 64)
-        err = launch_cluster_any<16, 4, 4>(a, num_sms, s, launched);
+        err = launch_cluster_any<16, 4, 4, 1, 2>(a, num_sms, s, launched);
     if (launched) return err;
     // more than 64 experts, or a gate too large for a cluster of 8
     if (a.E <= 8) return launch_route_t<8, 4>(a, num_sms, s);
