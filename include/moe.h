@@ -108,7 +108,20 @@ enum {
      * Both give bit-identical results. */
     MOE_OPT_GEMM0_A = 0,
     MOE_GEMM0_A_PERMUTED = 0,
-    MOE_GEMM0_A_TMA_GATHER = 1
+    MOE_GEMM0_A_TMA_GATHER = 1,
+    /* Where moe_layer_forward sums the k weighted expert rows of a token:
+     *   MOE_COMBINE_AUTO     (default) fused when the last GEMM1 to run (the
+     *                        shared expert's if any, else the routed one) has
+     *                        K >= 4096, else separate;
+     *   MOE_COMBINE_FUSED    in GEMM1's epilogue: each row takes an integer
+     *                        ticket per (token, 256-column tile) and the last
+     *                        one sums the token's slots in rank order;
+     *   MOE_COMBINE_SEPARATE a streaming combine kernel after the GEMMs.
+     * Both sum the same fp32 values in the same order: bit-identical. */
+    MOE_OPT_COMBINE = 1,
+    MOE_COMBINE_AUTO = 0,
+    MOE_COMBINE_FUSED = 1,
+    MOE_COMBINE_SEPARATE = 2
 };
 
 /* Sets a library-wide option for later calls (all devices and threads).

@@ -96,6 +96,11 @@ def test_options(L):
     assert L.moe_set_option(0, 7) == 1
     assert L.moe_set_option(3, 0) == 1
     assert L.moe_get_option(3) == -1
+    assert lib.get_combine() == lib.COMBINE_AUTO
+    for mode in (lib.COMBINE_FUSED, lib.COMBINE_SEPARATE, lib.COMBINE_AUTO):
+        lib.set_combine(mode)
+        assert lib.get_combine() == mode
+    assert L.moe_set_option(1, 3) == 1
 
 
 def test_zero_tokens_is_noop_on_host(L):

@@ -241,6 +241,41 @@ def test_small_case_tma_gather(lib, oracle, tma_gather, name):
     run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=1, tol="elementwise")
 
 
+@pytest.mark.parametrize("shape", [(300, 256, 192, 8, 2, 0), (257, 192, 128, 64, 6, 0),
+                                   (200, 256, 128, 16, 4, 384), (64, 128, 64, 256, 8, 0)])
+def test_combine_forms_bit_identical(lib, shape):
+    """The combine fused into GEMM1 (last contribution sums the slots) and the
+    separate combine kernel give bit-identical outputs, whatever the order in
+    which the contributions arrive."""
+    T, H, F, E, k, Fs = shape
+    inp = make_inputs(T, H, F, E, Fs=Fs, seed=9)
+    g = {n: v.cuda() for n, v in inp.items()}
+    dims = lib.make_dims(T, H, F, E, k, Fs)
+    ws = lib.workspace(dims)
+    outs = []
+    for mode in (lib.COMBINE_SEPARATE, lib.COMBINE_FUSED, lib.COMBINE_FUSED):
+        lib.set_combine(mode)
+        try:
+            outs.append(lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws,
+                                          W1s=g.get("W1s"), W3s=g.get("W3s"), W2s=g.get("W2s")).clone())
+        finally:
+            lib.set_combine(lib.COMBINE_AUTO)
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+@pytest.mark.parametrize("name", ["tiny", "f_tail", "h_tail_e64", "shared", "e256"])
+def test_small_case_fused_combine(lib, oracle, name):
+    """Edge cases with the combine fused into GEMM1 forced on."""
+    lib.set_combine(lib.COMBINE_FUSED)
+    try:
+        T, H, F, E, k, Fs = SMALL_CASES[name]
+        run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=1, tol="elementwise")
+    finally:
+        lib.set_combine(lib.COMBINE_AUTO)
+
+
 def test_gather_paths_bit_identical(lib):
     """Both ways of feeding GEMM0 give bit-identical layer outputs."""
     T, H, F, E, k, Fs = 900, 384, 320, 16, 4, 192

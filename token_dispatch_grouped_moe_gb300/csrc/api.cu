@@ -23,6 +23,7 @@ constexpr int kMaxDevices = 64;
 
 std::atomic<int> g_num_sms[kMaxDevices];
 std::atomic<int> g_gemm0_a{MOE_GEMM0_A_PERMUTED};
+std::atomic<int> g_combine{MOE_COMBINE_AUTO};
 
 int num_sms_current()
 {
@@ -88,7 +89,7 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, total;
+    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, arrive, total;
 };
 
 Layout layout_of(const moe_dims& d)
@@ -110,6 +111,7 @@ Layout layout_of(const moe_dims& d)
     L.h = o; o += al256(R * (size_t)d.F * 2);
     L.hs = o; o += al256(T * (size_t)d.F_shared * 2);
     L.slot = o; o += al256(((size_t)d.k + (d.F_shared > 0 ? 1 : 0)) * T * (size_t)d.H * 4);
+    L.arrive = o; o += al256(T * (size_t)((d.H + 255) / 256) * 4);
     L.total = o;
     return L;
 }
@@ -166,11 +168,22 @@ unsigned char* bytes(void* p) { return static_cast<unsigned char*>(p); }
 // The two grouped GEMMs of one expert set (routed or shared). GEMM0 reads its
 // A rows from x_rows ([M,H], already in dispatch order) when given, else it
 // gathers them from x with TMA gather4.
+// With `fused` (the layer path), GEMM1 also finishes the combine: slot is the
+// whole [n_slots, T, H] array, this launch writes slots slot_j0 .. slot_j0+k-1,
+// and the last contribution to each (token, 256-column tile) writes out.
+struct FusedCombine {
+    bool on;
+    int32_t slot_j0, n_slots;
+    int32_t* arrive;
+    uint16_t* out;
+};
+
 moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, int32_t k,
                             const uint16_t* x, const uint16_t* x_rows, const int32_t* src_row,
                             const int32_t* tile_start, const int32_t* offsets, const uint16_t* W1,
                             const uint16_t* W3, const uint16_t* W2, const float* topk_w, float* slot,
-                            uint16_t* h, uint32_t* err, int sms, cudaStream_t s, moe_event_t ev_mid)
+                            uint16_t* h, uint32_t* err, int sms, cudaStream_t s, moe_event_t ev_mid,
+                            const FusedCombine& fc = FusedCombine{false, 0, 0, nullptr, nullptr})
 {
     if (M == 0) {
         if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
@@ -207,7 +220,11 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
     a.h_out = nullptr;
     a.topk_w = topk_w;
     a.slot = slot;
-    MOE_TRY(launch_grouped_gemm(kGemm1Scatter, mh, m2, m2, a, sms, s));
+    a.slot_j0 = fc.on ? fc.slot_j0 : 0;
+    a.n_slots = fc.n_slots;
+    a.arrive = fc.arrive;
+    a.out = fc.out;
+    MOE_TRY(launch_grouped_gemm(fc.on ? kGemm1Combine : kGemm1Scatter, mh, m2, m2, a, sms, s));
     return MOE_OK;
 }
 
@@ -241,16 +258,25 @@ const char* moe_status_string(int status)
 
 moe_status moe_set_option(int option, int value)
 {
-    if (option != MOE_OPT_GEMM0_A) return MOE_ERR_INVALID_ARG;
-    if (value != MOE_GEMM0_A_PERMUTED && value != MOE_GEMM0_A_TMA_GATHER) return MOE_ERR_INVALID_ARG;
-    g_gemm0_a.store(value);
-    return MOE_OK;
+    if (option == MOE_OPT_GEMM0_A) {
+        if (value != MOE_GEMM0_A_PERMUTED && value != MOE_GEMM0_A_TMA_GATHER) return MOE_ERR_INVALID_ARG;
+        g_gemm0_a.store(value);
+        return MOE_OK;
+    }
+    if (option == MOE_OPT_COMBINE) {
+        if (value != MOE_COMBINE_AUTO && value != MOE_COMBINE_FUSED && value != MOE_COMBINE_SEPARATE)
+            return MOE_ERR_INVALID_ARG;
+        g_combine.store(value);
+        return MOE_OK;
+    }
+    return MOE_ERR_INVALID_ARG;
 }
 
 int moe_get_option(int option)
 {
-    if (option != MOE_OPT_GEMM0_A) return -1;
-    return g_gemm0_a.load();
+    if (option == MOE_OPT_GEMM0_A) return g_gemm0_a.load();
+    if (option == MOE_OPT_COMBINE) return g_combine.load();
+    return -1;
 }
 
 size_t moe_workspace_size(const moe_dims* dims)
@@ -400,6 +426,16 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_bf16* x, const moe_
     int32_t* tile = reinterpret_cast<int32_t*>(w + L.tile);
     float* slot = reinterpret_cast<float*>(w + L.slot);
     const int64_t R = d.T * d.k;
+    const int32_t n_slots = d.k + (d.F_shared > 0 ? 1 : 0);
+    int32_t* arrive = reinterpret_cast<int32_t*>(w + L.arrive);
+    // Fused combine: measured faster when the last GEMM1's K loop is long
+    // (Mixtral F = 14336, Qwen2 shared F = 20480), slower for short tiles
+    // (DeepSeek F = 1408), where the epilogue is already the bottleneck.
+    const int combine_opt = g_combine.load();
+    const int32_t k_last = d.F_shared > 0 ? d.F_shared : d.F;
+    const bool fused = combine_opt == MOE_COMBINE_FUSED || (combine_opt == MOE_COMBINE_AUTO && k_last >= 4096);
+    if (fused)   // GEMM1 counts contributions per (token, 256-column tile)
+        MOE_TRY(cudaMemsetAsync(arrive, 0, (size_t)d.T * ((d.H + 255) / 256) * 4, s));
 
     record(events ? events->before_route : nullptr, s);
     RouteArgs ra{x, Wg, bias, idx, tw, d.T, d.H, d.E, d.k};
@@ -419,19 +455,22 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_bf16* x, const moe_
     MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)R, d.F, d.E, d.k, x, permuted ? xp : nullptr, src,
                                     tile, offsets, W1, W3, W2, tw, slot,
                                     reinterpret_cast<uint16_t*>(w + L.h), err, sms, s,
-                                    events ? events->before_gemm1 : nullptr));
+                                    events ? events->before_gemm1 : nullptr,
+                                    FusedCombine{fused, 0, n_slots, arrive, out}));
 
     record(events ? events->before_shared : nullptr, s);
     if (d.F_shared > 0) {
         // identity dispatch: every token, in token order, weight 1
         MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)d.T, d.F_shared, 1, 1, x, permuted ? x : nullptr,
                                         nullptr, nullptr, nullptr, W1s, W3s, W2s, nullptr,
-                                        slot + (size_t)d.k * d.T * d.H,
-                                        reinterpret_cast<uint16_t*>(w + L.hs), err, sms, s, nullptr));
+                                        fused ? slot : slot + (size_t)d.k * d.T * d.H,
+                                        reinterpret_cast<uint16_t*>(w + L.hs), err, sms, s, nullptr,
+                                        FusedCombine{fused, d.k, n_slots, arrive, out}));
     }
 
     record(events ? events->before_combine : nullptr, s);
-    MOE_TRY(launch_combine(slot, d.k + (d.F_shared > 0 ? 1 : 0), out, d.T, d.H, sms, s));
+    if (!fused)   // else GEMM1's epilogue finished it (the last contribution)
+        MOE_TRY(launch_combine(slot, n_slots, out, d.T, d.H, sms, s));
     record(events ? events->after_combine : nullptr, s);
     return finish(cudaSuccess, ws, s);
 }

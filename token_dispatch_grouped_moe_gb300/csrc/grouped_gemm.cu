@@ -26,6 +26,11 @@
 //     each row by its gate weight and writes it to slot[rank][token] (f32):
 //     every slot is written exactly once, so the later combine is a fixed
 //     rank-order sum with no float atomics.
+//   GEMM1 + combine (mode kGemm1Combine): the same, then each row takes an
+//     integer ticket for its (token, N tile); the row that takes the last of
+//     the n_slots tickets sums the token's slots in rank order (fp32, the
+//     same left fold as the separate combine kernel) and writes the bf16
+//     output. Which row is last depends on scheduling; the sum does not.
 //
 // Kernel shape: one CTA per SM (192 threads, ~197 KB of shared memory),
 // persistent over a static schedule of (expert, N tile, M tile) work items
@@ -111,7 +116,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     unsigned char* tiles = smem_raw + (tiles_addr - raw_addr);
     SmemTail* st = reinterpret_cast<SmemTail*>(tiles + (size_t)STAGES * STAGE_BYTES);
 
-    constexpr bool IS_GEMM0 = (MODE != kGemm1Scatter);
+    constexpr bool IS_GEMM0 = (MODE == kGemm0Gather || MODE == kGemm0Dense);
     constexpr bool GATHER = (MODE == kGemm0Gather);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -339,7 +344,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         wt = args.topk_w[f];
                     }
                 }
-                float* dst_row = args.slot + ((int64_t)j * args.T + t) * args.N + n0;
+                float* dst_row = args.slot + ((int64_t)(args.slot_j0 + j) * args.T + t) * args.N + n0;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t v[32];
@@ -361,7 +366,54 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&st->tempty[acc]));
+            if (lane == 0) mbar_arrive(smem_u32(&st->tempty[acc]));   // TMEM free for the MMA
+            if constexpr (MODE == kGemm1Combine) {
+                // publish this row's slot segment, then take a ticket for its
+                // (token, N tile); the holder of the last ticket finishes it
+                int64_t t = -1;
+                bool last = false;
+                if (valid) {
+                    const int f = args.src_row ? args.src_row[p] : p;
+                    if (f >= 0 && f / args.k < args.T) {
+                        t = f / args.k;
+                        __threadfence();
+                        last = atomicAdd(args.arrive + t * n_tiles + wk.n_tile, 1) == args.n_slots - 1;
+                    }
+                }
+                // the warp sums its finished rows together: lane l takes columns
+                // 8l .. 8l+7, so each slot row is read as one coalesced 1 KB line
+                unsigned todo = __ballot_sync(0xffffffffu, last);
+                if (todo) __threadfence();
+                const int n0 = wk.n_tile * BN;
+                const int c = 8 * lane;
+                const int64_t TN = args.T * (int64_t)args.N;
+                while (todo) {
+                    const int src_lane = __ffs(todo) - 1;
+                    todo &= todo - 1;
+                    const int64_t tt = __shfl_sync(0xffffffffu, t, src_lane);
+                    if (n0 + c < args.N) {
+                        const float* src = args.slot + tt * args.N + n0 + c;
+                        float4 a0 = __ldcg(reinterpret_cast<const float4*>(src));
+                        float4 a1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
+                        for (int jj = 1; jj < args.n_slots; ++jj) {
+                            const float4 b0 = __ldcg(reinterpret_cast<const float4*>(src + jj * TN));
+                            const float4 b1 = __ldcg(reinterpret_cast<const float4*>(src + jj * TN + 4));
+                            a0.x = a0.x + b0.x; a0.y = a0.y + b0.y; a0.z = a0.z + b0.z; a0.w = a0.w + b0.w;
+                            a1.x = a1.x + b1.x; a1.y = a1.y + b1.y; a1.z = a1.z + b1.z; a1.w = a1.w + b1.w;
+                        }
+                        __nv_bfloat162 p0 = __floats2bfloat162_rn(a0.x, a0.y);
+                        __nv_bfloat162 p1 = __floats2bfloat162_rn(a0.z, a0.w);
+                        __nv_bfloat162 p2 = __floats2bfloat162_rn(a1.x, a1.y);
+                        __nv_bfloat162 p3 = __floats2bfloat162_rn(a1.z, a1.w);
+                        uint4 o;
+                        o.x = *reinterpret_cast<uint32_t*>(&p0);
+                        o.y = *reinterpret_cast<uint32_t*>(&p1);
+                        o.z = *reinterpret_cast<uint32_t*>(&p2);
+                        o.w = *reinterpret_cast<uint32_t*>(&p3);
+                        *reinterpret_cast<uint4*>(args.out + tt * args.N + n0 + c) = o;
+                    }
+                }
+            }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
     }
@@ -388,6 +440,7 @@ cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensor
     if (mode == kGemm0Gather) kern = grouped_gemm_kernel<kGemm0Gather>;
     else if (mode == kGemm0Dense) kern = grouped_gemm_kernel<kGemm0Dense>;
     else if (mode == kGemm1Scatter) kern = grouped_gemm_kernel<kGemm1Scatter>;
+    else if (mode == kGemm1Combine) kern = grouped_gemm_kernel<kGemm1Combine>;
     else return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;

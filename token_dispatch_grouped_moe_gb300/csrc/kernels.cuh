@@ -48,8 +48,10 @@ cudaError_t launch_tile_table(const int32_t* offsets, int32_t G, int32_t* tile_s
                               cudaStream_t s);
 
 // GEMM0 + SwiGLU with A gathered from x by TMA gather4 (kGemm0Gather) or read
-// from the dispatch-ordered copy x_perm (kGemm0Dense); GEMM1 + weighted scatter.
-enum GemmMode { kGemm0Gather = 0, kGemm1Scatter = 1, kGemm0Dense = 2 };
+// from the dispatch-ordered copy x_perm (kGemm0Dense); GEMM1 + weighted scatter
+// (kGemm1Scatter), or GEMM1 + weighted scatter + the combine done by the last
+// of the n_slots contributions to each (token, 256-column tile) (kGemm1Combine).
+enum GemmMode { kGemm0Gather = 0, kGemm1Scatter = 1, kGemm0Dense = 2, kGemm1Combine = 3 };
 
 struct GemmArgs {
     int32_t M;                   // rows in dispatched order (R, or T for a dense expert)
@@ -63,7 +65,11 @@ struct GemmArgs {
     const int32_t* src_row;      // [M] or null (identity)
     const float* topk_w;         // GEMM1: [M] by f, or null (weight 1)
     __nv_bfloat16* h_out;        // GEMM0: [M, N]
-    float* slot;                 // GEMM1: [k, T, N]
+    float* slot;                 // GEMM1: slot array [n_slots, T, N]; rank j goes to slot_j0 + j
+    int32_t slot_j0;             // GEMM1: first slot of this launch (the shared expert: k)
+    int32_t n_slots;             // kGemm1Combine: contributions summed per (token, N tile)
+    int32_t* arrive;             // kGemm1Combine: [T, ceil(N/256)] tickets, zero before the first launch
+    uint16_t* out;               // kGemm1Combine: [T, N] bf16 layer output
     uint32_t* err;
 };
 

@@ -27,6 +27,10 @@ EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check"
 OPT_GEMM0_A = 0
 GEMM0_A_PERMUTED = 0      # dispatch copies token rows to x_perm; GEMM0 loads dense tiles
 GEMM0_A_TMA_GATHER = 1    # GEMM0 producer gathers token rows with TMA gather4
+OPT_COMBINE = 1
+COMBINE_AUTO = 0          # fused when the last GEMM1 has K >= 4096
+COMBINE_FUSED = 1         # GEMM1's epilogue: the last contribution sums the slots
+COMBINE_SEPARATE = 2      # a streaming combine kernel after the GEMMs
 
 
 class MoeError(RuntimeError):
@@ -115,6 +119,15 @@ def set_gemm0_a(mode: int) -> None:
 
 def get_gemm0_a() -> int:
     return int(load().moe_get_option(OPT_GEMM0_A))
+
+
+def set_combine(mode: int) -> None:
+    """Choose where the layer sums the expert rows (COMBINE_AUTO / _FUSED / _SEPARATE)."""
+    _ok(load().moe_set_option(OPT_COMBINE, int(mode)), "moe_set_option")
+
+
+def get_combine() -> int:
+    return int(load().moe_get_option(OPT_COMBINE))
 
 
 def make_dims(T, H, F, E, k, F_shared=0) -> Dims:
