@@ -32,6 +32,12 @@
  *          silu(a) = a / (1 + exp(-a)); W1 is under the silu;
  *       R5 the combine sums w_j * y_j over ranks j = 0..k-1 in rank order,
  *          then adds the always-on shared expert (weight 1) when present.
+ *     Two gating variants (readings too; the pages have neither):
+ *       R3' no renormalisation: w_j is the softmax of logit j over all E
+ *          experts, so the k weights sum to less than 1 (unless k = E);
+ *       R5' sigmoid-gated shared expert: the shared expert's output is
+ *          scaled by s(x) = 1 / (1 + exp(-x . wsg)) for a gate vector wsg[H]
+ *          (x . wsg in fp64) instead of 1.
  *
  * Precision. Every input is bf16 and is widened to float exactly. The
  * logits (which decide integers: the expert ids) are computed in fp32 in the
@@ -166,6 +172,39 @@ int oracle_route(int64_t T, int32_t H, int32_t E, int32_t k, const uint16_t* x,
     return oracle_topk(T, E, k, logits, topk_idx, topk_w);
 }
 
+/* Reading R3': gate weights without renormalisation, from the logits and the
+ * selected ids: w_j = exp(l_j - m) / sum over all E experts of exp(l_e - m),
+ * m the largest logit (rank 0's), in fp64, rounded once to fp32. */
+int oracle_gate_weights_full(int64_t T, int32_t E, int32_t k, const float* logits,
+                             const int32_t* topk_idx, float* topk_w)
+{
+    if (T < 0 || E <= 0 || k <= 0 || k > E || (T > 0 && (!logits || !topk_idx || !topk_w)))
+        return ORACLE_BAD_ARG;
+    for (int64_t t = 0; t < T; ++t) {
+        const float* l = logits + t * E;
+        double m = (double)l[topk_idx[t * k]];
+        double den_all = 0.0;
+        for (int32_t e = 0; e < E; ++e) den_all += exp((double)l[e] - m);
+        for (int32_t j = 0; j < k; ++j)
+            topk_w[t * k + j] = (float)(exp((double)l[topk_idx[t * k + j]] - m) / den_all);
+    }
+    return ORACLE_OK;
+}
+
+/* Reading R5': the shared expert's scale s[t] = 1 / (1 + exp(-x[t] . wsg)),
+ * the dot product in fp64 in increasing h. */
+int oracle_shared_gate(int64_t T, int32_t H, const uint16_t* x, const uint16_t* wsg, double* scale)
+{
+    if (T < 0 || H <= 0 || (T > 0 && (!x || !wsg || !scale))) return ORACLE_BAD_ARG;
+    for (int64_t t = 0; t < T; ++t) {
+        double d = 0.0;
+        for (int32_t h = 0; h < H; ++h)
+            d += (double)bf16_to_float(x[t * H + h]) * (double)bf16_to_float(wsg[h]);
+        scale[t] = 1.0 / (1.0 + exp(-d));
+    }
+    return ORACLE_OK;
+}
+
 /* -------------------------------------------------------------- permute -- */
 
 /*
@@ -248,7 +287,8 @@ int oracle_expert_row(int32_t H, int32_t F, const uint16_t* xrow, const uint16_t
 }
 
 /*
- * Layer output for a list of tokens (reading R5):
+ * Layer output for a list of tokens (reading R5; R5' when shared_scale, [T],
+ * is given):
  *   out[i,:] = sum_{j=0..k-1} topk_w[t,j] * FFN_{topk_idx[t,j]}(x[t])
  *              (+ FFN_shared(x[t]) when Fs > 0),  t = tokens[i]
  * summed in rank order j = 0..k-1, the shared expert last.
@@ -257,11 +297,12 @@ int oracle_expert_row(int32_t H, int32_t F, const uint16_t* xrow, const uint16_t
  * The (token, expert) FFNs run in parallel; the sums run in the order above.
  * W1, W3 are [E,H,F], W2 is [E,F,H]; W1s, W3s are [H,Fs], W2s is [Fs,H].
  */
-int oracle_layer_rows(int64_t T, int32_t H, int32_t F, int32_t E, int32_t k, int32_t Fs,
-                      const int64_t* tokens, int64_t n_tok, const int32_t* topk_idx,
-                      const float* topk_w, const uint16_t* x, const uint16_t* W1,
-                      const uint16_t* W3, const uint16_t* W2, const uint16_t* W1s,
-                      const uint16_t* W3s, const uint16_t* W2s, double* out)
+int oracle_layer_rows_gated(int64_t T, int32_t H, int32_t F, int32_t E, int32_t k, int32_t Fs,
+                            const int64_t* tokens, int64_t n_tok, const int32_t* topk_idx,
+                            const float* topk_w, const uint16_t* x, const uint16_t* W1,
+                            const uint16_t* W3, const uint16_t* W2, const uint16_t* W1s,
+                            const uint16_t* W3s, const uint16_t* W2s, const double* shared_scale,
+                            double* out)
 {
     if (T < 0 || H <= 0 || F <= 0 || E <= 0 || k <= 0 || k > E || Fs < 0 || n_tok < 0)
         return ORACLE_BAD_ARG;
@@ -317,9 +358,25 @@ int oracle_layer_rows(int64_t T, int32_t H, int32_t F, int32_t E, int32_t k, int
         }
         if (Fs > 0) {
             const double* y = ys + (i * per_tok + k) * (int64_t)H;
-            for (int32_t n = 0; n < H; ++n) o[n] += y[n];
+            if (!shared_scale) {
+                for (int32_t n = 0; n < H; ++n) o[n] += y[n];
+            } else {
+                double sc = shared_scale[t];   /* reading R5' */
+                for (int32_t n = 0; n < H; ++n) o[n] += sc * y[n];
+            }
         }
     }
     free(ys);
     return ORACLE_OK;
+}
+
+/* The layer rows with the always-on shared expert at weight 1 (reading R5). */
+int oracle_layer_rows(int64_t T, int32_t H, int32_t F, int32_t E, int32_t k, int32_t Fs,
+                      const int64_t* tokens, int64_t n_tok, const int32_t* topk_idx,
+                      const float* topk_w, const uint16_t* x, const uint16_t* W1,
+                      const uint16_t* W3, const uint16_t* W2, const uint16_t* W1s,
+                      const uint16_t* W3s, const uint16_t* W2s, double* out)
+{
+    return oracle_layer_rows_gated(T, H, F, E, k, Fs, tokens, n_tok, topk_idx, topk_w, x, W1, W3,
+                                   W2, W1s, W3s, W2s, NULL, out);
 }

@@ -49,6 +49,13 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_topk.argtypes = [i64, i32, i32, P, P, P]
     lib.oracle_route.restype = ctypes.c_int
     lib.oracle_route.argtypes = [i64, i32, i32, i32, P, P, P, P, P, P]
+    lib.oracle_gate_weights_full.restype = ctypes.c_int
+    lib.oracle_gate_weights_full.argtypes = [i64, i32, i32, P, P, P]
+    lib.oracle_shared_gate.restype = ctypes.c_int
+    lib.oracle_shared_gate.argtypes = [i64, i32, P, P, P]
+    lib.oracle_layer_rows_gated.restype = ctypes.c_int
+    lib.oracle_layer_rows_gated.argtypes = [i64, i32, i32, i32, i32, i32, P, i64, P, P,
+                                            P, P, P, P, P, P, P, P, P]
     lib.oracle_permute.restype = ctypes.c_int
     lib.oracle_permute.argtypes = [i64, i32, P, P, P, P, P]
     lib.oracle_expert_row.restype = ctypes.c_int
@@ -114,6 +121,25 @@ class Oracle:
         _check(self.lib.oracle_topk(T, E, k, _ptr(logits), _ptr(idx), _ptr(w)), "topk")
         return idx, w
 
+    def gate_weights_full(self, logits, topk_idx) -> np.ndarray:
+        """Weights without renormalisation (softmax over all E at the selected ids)."""
+        logits = np.ascontiguousarray(logits, dtype=np.float32)
+        idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+        T, E = logits.shape
+        k = idx.shape[1]
+        w = np.empty((T, k), np.float32)
+        _check(self.lib.oracle_gate_weights_full(T, E, k, _ptr(logits), _ptr(idx), _ptr(w)),
+               "gate_weights_full")
+        return w
+
+    def shared_gate(self, x, wsg) -> np.ndarray:
+        """s[t] = sigmoid(x[t] . wsg) (fp64)."""
+        x, wsg = _u16(x), _u16(wsg)
+        T, H = x.shape
+        out = np.empty(T, np.float64)
+        _check(self.lib.oracle_shared_gate(T, H, _ptr(x), _ptr(wsg), _ptr(out)), "shared_gate")
+        return out
+
     def route(self, x, Wg, k: int, bias=None):
         """Returns (logits[T,E] f32, topk_idx[T,k] i32, topk_w[T,k] f32)."""
         x, Wg = _u16(x), _u16(Wg)
@@ -148,8 +174,9 @@ class Oracle:
         return y
 
     def layer_rows(self, tokens, topk_idx, topk_w, x, W1, W3, W2, W1s=None, W3s=None,
-                   W2s=None) -> np.ndarray:
-        """out[len(tokens), H] (fp64) for the listed tokens, given the routing."""
+                   W2s=None, shared_scale=None) -> np.ndarray:
+        """out[len(tokens), H] (fp64) for the listed tokens, given the routing;
+        shared_scale[T] (fp64) scales the shared expert (default 1)."""
         x, W1, W3, W2 = _u16(x), _u16(W1), _u16(W3), _u16(W2)
         T, H = x.shape
         E, _, F = W1.shape
@@ -162,23 +189,36 @@ class Oracle:
         idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
         w = np.ascontiguousarray(topk_w, dtype=np.float32)
         out = np.empty((tokens.size, H), np.float64)
-        _check(self.lib.oracle_layer_rows(T, H, F, E, k, Fs, _ptr(tokens), tokens.size, _ptr(idx),
-                                          _ptr(w), _ptr(x), _ptr(W1), _ptr(W3), _ptr(W2),
-                                          _ptr(W1s), _ptr(W3s), _ptr(W2s), _ptr(out)),
-               "layer_rows")
+        if shared_scale is None:
+            _check(self.lib.oracle_layer_rows(T, H, F, E, k, Fs, _ptr(tokens), tokens.size, _ptr(idx),
+                                              _ptr(w), _ptr(x), _ptr(W1), _ptr(W3), _ptr(W2),
+                                              _ptr(W1s), _ptr(W3s), _ptr(W2s), _ptr(out)),
+                   "layer_rows")
+        else:
+            sc = np.ascontiguousarray(shared_scale, dtype=np.float64)
+            _check(self.lib.oracle_layer_rows_gated(T, H, F, E, k, Fs, _ptr(tokens), tokens.size,
+                                                    _ptr(idx), _ptr(w), _ptr(x), _ptr(W1), _ptr(W3),
+                                                    _ptr(W2), _ptr(W1s), _ptr(W3s), _ptr(W2s),
+                                                    _ptr(sc), _ptr(out)),
+                   "layer_rows_gated")
         return out
 
     def layer_forward(self, x, Wg, W1, W3, W2, k: int, bias=None, W1s=None, W3s=None, W2s=None,
-                      tokens=None):
+                      tokens=None, renormalize=True, wsg=None):
         """Route, then the output rows for ``tokens`` (all tokens by default).
+        renormalize=False takes the weights over all E (reading R3'); wsg gates
+        the shared expert with sigmoid(x . wsg) (reading R5').
 
         Returns a dict with logits, topk_idx, topk_w, counts, offsets, src_row,
         inv_pos, tokens and out (fp64)."""
         logits, idx, w = self.route(x, Wg, k, bias)
+        if not renormalize:
+            w = self.gate_weights_full(logits, idx)
+        scale = None if wsg is None else self.shared_gate(x, wsg)
         E = Wg.shape[1]
         counts, offsets, src_row, inv_pos = self.permute(idx, E)
         if tokens is None:
             tokens = np.arange(x.shape[0], dtype=np.int64)
-        out = self.layer_rows(tokens, idx, w, x, W1, W3, W2, W1s, W3s, W2s)
+        out = self.layer_rows(tokens, idx, w, x, W1, W3, W2, W1s, W3s, W2s, shared_scale=scale)
         return dict(logits=logits, topk_idx=idx, topk_w=w, counts=counts, offsets=offsets,
                     src_row=src_row, inv_pos=inv_pos, tokens=np.asarray(tokens), out=out)

@@ -331,6 +331,47 @@ def pin_worked_example(O):
     assert r["src_row"].tolist() == [1, 2, 0, 3]      # f = t*k + j, grouped by expert
 
 
+# ------------------------------------------------------- gating variants --
+
+def pin_gate_weights_full(O):
+    """Without renormalisation the weights are a softmax over all E experts
+    (numpy fp64) at the selected ids; they sum to less than 1, and to 1 when
+    k = E, where they equal the renormalised weights."""
+    rng = np.random.default_rng(15)
+    for E, k in [(8, 2), (64, 6), (5, 5)]:
+        logits = (rng.standard_normal((40, E)) * 1.5).astype(np.float32)
+        idx, w_renorm = O.topk(logits, k)
+        w = O.gate_weights_full(logits, idx)
+        l64 = logits.astype(np.float64)
+        p = np.exp(l64 - l64.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        ref = np.take_along_axis(p, idx.astype(np.int64), axis=1)
+        assert np.allclose(w, ref, rtol=1e-6, atol=1e-8)
+        if k < E:
+            assert np.all(w.astype(np.float64).sum(axis=1) < 1.0)
+        else:
+            assert np.allclose(w, w_renorm, rtol=1e-6, atol=1e-8)
+
+
+def pin_shared_gate(O):
+    """The sigmoid-gated shared expert: wsg = 0 gives exactly half the shared
+    expert; random wsg scales it by torch's sigmoid(x @ wsg) (fp64)."""
+    T, H, F, E, k, Fs = 10, 64, 32, 4, 2, 80
+    inp = make_inputs(T, H, F, E, Fs=Fs, seed=16)
+    b = {n: bf16_bits(v) for n, v in inp.items()}
+    args = (b["x"], b["Wg"], b["W1"], b["W3"], b["W2"])
+    without = O.layer_forward(*args, k=k)["out"]
+    dense = _swiglu_torch(_t64(b["x"]), _t64(b["W1s"]), _t64(b["W3s"]), _t64(b["W2s"])).numpy()
+    zero = np.zeros(H, np.uint16)
+    half = O.layer_forward(*args, k=k, W1s=b["W1s"], W3s=b["W3s"], W2s=b["W2s"], wsg=zero)["out"]
+    scale = float(np.sqrt(np.mean(dense ** 2)))
+    assert np.max(np.abs((half - without) - 0.5 * dense)) <= 1e-9 * scale
+    wsg = _rand_bits((H,), np.random.default_rng(17), 0.05)
+    gated = O.layer_forward(*args, k=k, W1s=b["W1s"], W3s=b["W3s"], W2s=b["W2s"], wsg=wsg)["out"]
+    s = torch.sigmoid(_t64(b["x"]) @ _t64(wsg)).numpy()
+    assert np.max(np.abs((gated - without) - s[:, None] * dense)) <= 1e-9 * scale
+
+
 ALL_PINS = [
     pin_logits_exact_integers,
     pin_logits_canonical_order,
@@ -346,4 +387,6 @@ ALL_PINS = [
     pin_shared_expert,
     pin_row_independence,
     pin_worked_example,
+    pin_gate_weights_full,
+    pin_shared_gate,
 ]

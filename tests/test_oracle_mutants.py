@@ -35,6 +35,11 @@ MUTANTS = {
                       "y[n] += gv * (double)bf16_to_float(W2[(int64_t)n * F + f]);"),
     "expert_stride": ("W1 + e * H * (int64_t)F, W3 + e * H * (int64_t)F",
                       "W1 + e * (int64_t)F, W3 + e * H * (int64_t)F"),
+    "full_softmax_over_k_only": ("for (int32_t e = 0; e < E; ++e) den_all += exp((double)l[e] - m);",
+                                 "for (int32_t e = 0; e < k; ++e) den_all += exp((double)l[topk_idx[t * k + e]] - m);"),
+    "shared_gate_sign": ("scale[t] = 1.0 / (1.0 + exp(-d));", "scale[t] = 1.0 / (1.0 + exp(d));"),
+    "shared_gate_dropped": ("for (int32_t n = 0; n < H; ++n) o[n] += sc * y[n];",
+                            "for (int32_t n = 0; n < H; ++n) o[n] += y[n];"),
     "x_row_stride": ("const uint16_t* xrow = x + t * (int64_t)H;\n                double* y",
                      "const uint16_t* xrow = x + (t / k) * (int64_t)H;\n                double* y"),
 }
