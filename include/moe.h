@@ -86,6 +86,16 @@ typedef struct {
     moe_event_t after_combine;
 } moe_stage_events;
 
+/* Gating variants (readings of this library; the pages give no gate formula).
+ * A null moe_gating* means {renormalize = 1, shared_gate = NULL}. */
+typedef struct {
+    int32_t renormalize;          /* 1: weights = softmax over the k selected logits;
+                                     0: softmax over all E logits at the selected ids
+                                        (the k weights then sum to less than 1) */
+    const moe_bf16* shared_gate;  /* [H] or NULL: scale the shared expert's output by
+                                     sigmoid(x[t] . shared_gate) instead of 1 */
+} moe_gating;
+
 /* Optional routing outputs of moe_layer_forward; each null field is kept in
  * the workspace instead. Sizes: [T*k], [T*k], [E], [E+1], [T*k], [T*k]. */
 typedef struct {
@@ -156,6 +166,10 @@ moe_status moe_check(void* ws, moe_stream_t stream);
  */
 moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg, const float* bias,
                      int32_t* topk_idx, float* topk_w, moe_stream_t stream);
+
+/* moe_route with a gating variant (gating->renormalize; shared_gate unused). */
+moe_status moe_route_ex(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg, const float* bias,
+                        const moe_gating* gating, int32_t* topk_idx, float* topk_w, moe_stream_t stream);
 
 /*
  * Dispatch: stable counting sort of the R = T*k assignments f = t*k + j by
@@ -238,6 +252,15 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_bf16* x, const moe_
                              const moe_bf16* W2s, moe_bf16* out, const moe_routing_out* routing,
                              void* ws, size_t ws_bytes, const moe_stage_events* events,
                              moe_stream_t stream);
+
+/* moe_layer_forward with a gating variant (nullable; see moe_gating). A
+ * shared_gate needs F_shared > 0; its [H] vector must be 16-byte aligned. */
+moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg,
+                                const float* bias, const moe_gating* gating, const moe_bf16* W1,
+                                const moe_bf16* W3, const moe_bf16* W2, const moe_bf16* W1s,
+                                const moe_bf16* W3s, const moe_bf16* W2s, moe_bf16* out,
+                                const moe_routing_out* routing, void* ws, size_t ws_bytes,
+                                const moe_stage_events* events, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

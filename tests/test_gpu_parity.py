@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from token_dispatch_grouped_moe_gb300.configs import CONFIGS
-from token_dispatch_grouped_moe_gb300.inputs import bf16_bits, make_inputs
+from token_dispatch_grouped_moe_gb300.inputs import bf16_bits, bits_to_bf16, make_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -81,7 +81,7 @@ def elementwise_bound(tokens, idx, w, b, ref, Fs):
 
 
 def run_case(lib, oracle, T, H, F, E, k, Fs=0, seed=0, bias=None, sample=None, check_perm=True,
-             tol="config"):
+             tol="config", renormalize=True, wsg=None):
     """Runs the layer on the GPU and the oracle on the CPU and compares.
 
     tol="config": the layer configurations' bar, max |out - ref| <= 2e-2 rms(ref).
@@ -96,12 +96,17 @@ def run_case(lib, oracle, T, H, F, E, k, Fs=0, seed=0, bias=None, sample=None, c
     dims = lib.make_dims(T, H, F, E, k, Fs)
     ws = lib.workspace(dims, device=dev)
     routing = lib.routing_buffers(dims, dev)
+    wsg_t = None if wsg is None else bits_to_bf16(wsg).to(dev)
     out = lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws, bias=bias_t,
-                            W1s=g.get("W1s"), W3s=g.get("W3s"), W2s=g.get("W2s"), routing=routing)
+                            W1s=g.get("W1s"), W3s=g.get("W3s"), W2s=g.get("W2s"), routing=routing,
+                            renormalize=renormalize, shared_gate=wsg_t)
     torch.cuda.synchronize()
     assert lib.check(ws) == lib.MOE_OK
     # routing and dispatch: the oracle on every token
     logits, idx, w = oracle.route(b["x"], b["Wg"], k, bias)
+    if not renormalize:
+        w = oracle.gate_weights_full(logits, idx)
+    scale = None if wsg is None else oracle.shared_gate(b["x"], wsg)
     assert np.array_equal(routing.topk_idx.cpu().numpy(), idx), "top-k ids differ"
     gw = routing.topk_w.cpu().numpy()
     assert np.allclose(gw, w, rtol=TOL_W, atol=1e-7), f"gate weights differ: {np.max(np.abs(gw - w))}"
@@ -118,7 +123,7 @@ def run_case(lib, oracle, T, H, F, E, k, Fs=0, seed=0, bias=None, sample=None, c
         rng = np.random.default_rng(seed + 99)
         tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, sample, replace=False)]))
     ref = oracle.layer_rows(tokens, idx, w, b["x"], b["W1"], b["W3"], b["W2"], b.get("W1s"),
-                            b.get("W3s"), b.get("W2s"))
+                            b.get("W3s"), b.get("W2s"), shared_scale=scale)
     o = out.float().cpu().numpy()[tokens].astype(np.float64)
     rms = float(np.sqrt(np.mean(ref ** 2)))
     err = float(np.max(np.abs(o - ref)))
@@ -213,6 +218,41 @@ def test_route_bias_added_after_sum(lib):
     idx, _ = lib.route(dims, x.bfloat16().cuda(), Wg.bfloat16().cuda(), bias=bias.cuda())
     torch.cuda.synchronize()
     assert idx.cpu().tolist()[0] == [0, 1]
+
+
+def _wsg(H, seed):
+    t = (torch.from_numpy(np.random.default_rng(seed).standard_normal(H).astype(np.float32)) * 0.05)
+    return bf16_bits(t.to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("name", ["tiny", "h_tail_e64", "k_eq_e", "e256", "shared"])
+def test_gating_no_renormalisation(lib, oracle, name):
+    """Weights as a softmax over all E experts (not renormalised over the k)."""
+    T, H, F, E, k, Fs = SMALL_CASES[name]
+    run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=2, tol="elementwise", renormalize=False)
+
+
+@pytest.mark.parametrize("combine", ["fused", "separate"])
+def test_gating_sigmoid_shared(lib, oracle, combine):
+    """The shared expert scaled by sigmoid(x . wsg), with both combine forms."""
+    lib.set_combine(lib.COMBINE_FUSED if combine == "fused" else lib.COMBINE_SEPARATE)
+    try:
+        T, H, F, E, k, Fs = 300, 256, 128, 16, 4, 384
+        run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=3, tol="elementwise", renormalize=False,
+                 wsg=_wsg(H, 5))
+    finally:
+        lib.set_combine(lib.COMBINE_AUTO)
+
+
+def test_gating_shared_gate_needs_shared_expert(lib):
+    dims = lib.make_dims(8, 64, 64, 4, 2)
+    ws = lib.workspace(dims)
+    z = torch.zeros(64, dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros(8, 64, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(4, 64, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lib.MoeError):
+        lib.layer_forward(dims, x, torch.zeros(64, 4, dtype=torch.bfloat16, device="cuda"), W, W, W, ws,
+                          shared_gate=z)
 
 
 def test_zipf_bias_small(lib, oracle):
@@ -376,6 +416,18 @@ def test_zero_tokens(lib):
 # ----------------------------------------------------------- full sizes --
 
 FULL = ["mixtral", "qwen2", "dsk-1k", "dsk-4k", "dsk-16k", "dsk-32k", "mixtral-zipf"]
+
+
+@pytest.mark.slow
+def test_full_qwen2_gating_variants(lib, oracle):
+    """The Qwen2-shaped layer with its model family's gating: no
+    renormalisation and a sigmoid-gated shared expert. A variant beyond the
+    stated configurations, so the per-element arithmetic bound applies (its
+    output is dominated by the 20480-wide shared expert; err/rms measured
+    0.025, at the bf16 format's edge like the other extension shapes)."""
+    c = CONFIGS["qwen2"]
+    run_case(lib, oracle, c.T, c.H, c.F, c.E, c.k, Fs=c.Fs, seed=c.seed, sample=48,
+             renormalize=False, wsg=_wsg(c.H, 7), tol="elementwise")
 
 
 @pytest.mark.slow

@@ -89,7 +89,7 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, arrive, total;
+    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, arrive, sgate, total;
 };
 
 Layout layout_of(const moe_dims& d)
@@ -112,6 +112,7 @@ Layout layout_of(const moe_dims& d)
     L.hs = o; o += al256(T * (size_t)d.F_shared * 2);
     L.slot = o; o += al256(((size_t)d.k + (d.F_shared > 0 ? 1 : 0)) * T * (size_t)d.H * 4);
     L.arrive = o; o += al256(T * (size_t)((d.H + 255) / 256) * 4);
+    L.sgate = o; o += al256(T * 4);
     L.total = o;
     return L;
 }
@@ -302,6 +303,12 @@ moe_status moe_check(void* ws, moe_stream_t stream)
 moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg, const float* bias,
                      int32_t* topk_idx, float* topk_w, moe_stream_t stream)
 {
+    return moe_route_ex(dims, x, Wg, bias, nullptr, topk_idx, topk_w, stream);
+}
+
+moe_status moe_route_ex(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg, const float* bias,
+                        const moe_gating* gating, int32_t* topk_idx, float* topk_w, moe_stream_t stream)
+{
     MOE_TRY_STATUS(check_dims(dims));
     if (dims->T == 0) return MOE_OK;
     if (!x || !Wg || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
@@ -310,6 +317,7 @@ moe_status moe_route(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg
     if (sms <= 0) return MOE_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
     RouteArgs a{x, Wg, bias, topk_idx, topk_w, dims->T, dims->H, dims->E, dims->k};
+    a.renorm = gating ? (gating->renormalize != 0) : 1;
     return finish(launch_route(a, sms, s), nullptr, s);
 }
 
@@ -399,6 +407,17 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_bf16* x, const moe_
                              void* ws, size_t ws_bytes, const moe_stage_events* events,
                              moe_stream_t stream)
 {
+    return moe_layer_forward_ex(dims, x, Wg, bias, nullptr, W1, W3, W2, W1s, W3s, W2s, out, routing,
+                                ws, ws_bytes, events, stream);
+}
+
+moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg,
+                                const float* bias, const moe_gating* gating, const moe_bf16* W1,
+                                const moe_bf16* W3, const moe_bf16* W2, const moe_bf16* W1s,
+                                const moe_bf16* W3s, const moe_bf16* W2s, moe_bf16* out,
+                                const moe_routing_out* routing, void* ws, size_t ws_bytes,
+                                const moe_stage_events* events, moe_stream_t stream)
+{
     MOE_TRY_STATUS(check_dims(dims));
     MOE_TRY_STATUS(check_ws(*dims, ws, ws_bytes));
     const moe_dims& d = *dims;
@@ -410,6 +429,8 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_bf16* x, const moe_
         if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
     if (d.F_shared > 0 && (!aligned16(W1s) || !aligned16(W3s) || !aligned16(W2s)))
         return MOE_ERR_INVALID_ARG;
+    const moe_bf16* shared_gate = gating ? gating->shared_gate : nullptr;
+    if (shared_gate && (d.F_shared == 0 || !aligned16(shared_gate))) return MOE_ERR_INVALID_ARG;
     const int sms = num_sms_current();
     if (sms <= 0) return MOE_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
@@ -439,6 +460,7 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_bf16* x, const moe_
 
     record(events ? events->before_route : nullptr, s);
     RouteArgs ra{x, Wg, bias, idx, tw, d.T, d.H, d.E, d.k};
+    ra.renorm = gating ? (gating->renormalize != 0) : 1;
     MOE_TRY(launch_route(ra, sms, s));
 
     record(events ? events->before_permute : nullptr, s);
@@ -460,9 +482,15 @@ moe_status moe_layer_forward(const moe_dims* dims, const moe_bf16* x, const moe_
 
     record(events ? events->before_shared : nullptr, s);
     if (d.F_shared > 0) {
+        // the sigmoid gate, if any, is the shared expert's row weight in GEMM1
+        float* sgate = nullptr;
+        if (shared_gate) {
+            sgate = reinterpret_cast<float*>(w + L.sgate);
+            MOE_TRY(launch_shared_gate(x, shared_gate, sgate, d.T, d.H, sms, s));
+        }
         // identity dispatch: every token, in token order, weight 1
         MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)d.T, d.F_shared, 1, 1, x, permuted ? x : nullptr,
-                                        nullptr, nullptr, nullptr, W1s, W3s, W2s, nullptr,
+                                        nullptr, nullptr, nullptr, W1s, W3s, W2s, sgate,
                                         fused ? slot : slot + (size_t)d.k * d.T * d.H,
                                         reinterpret_cast<uint16_t*>(w + L.hs), err, sms, s, nullptr,
                                         FusedCombine{fused, d.k, n_slots, arrive, out}));

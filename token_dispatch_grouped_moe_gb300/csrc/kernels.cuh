@@ -20,8 +20,13 @@ struct RouteArgs {
     float* topk_w;         // [T,k]
     int64_t T;
     int32_t H, E, k;
+    int32_t renorm = 1;    // 1: softmax over the k selected; 0: over all E
 };
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s);
+
+// scale[t] = 1 / (1 + exp(-x[t] . wsg)) (the shared expert's sigmoid gate)
+cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* wsg, float* scale, int64_t T,
+                               int32_t H, int num_sms, cudaStream_t s);
 
 struct PermuteArgs {
     const int32_t* topk_idx;   // [R]

@@ -219,6 +219,13 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(RouteArgs a, in
                 sel_e[j < 8 ? j : 7] = be;
                 sel_l[j < 8 ? j : 7] = bv;
             }
+            // without renormalisation the denominator runs over all E experts
+            float den_all = 0.0f;
+            if (!a.renorm) {
+                for (int u = 0; lane + 32 * u < E; ++u) den_all += expf(l[lane + 32 * u] - sel_l[0]);
+#pragma unroll
+                for (int st = 16; st >= 1; st >>= 1) den_all += __shfl_xor_sync(0xffffffffu, den_all, st);
+            }
             if (lane == 0) {
                 const float m = sel_l[0];
                 float ex[8];
@@ -227,6 +234,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(RouteArgs a, in
                     ex[j] = expf(sel_l[j] - m);
                     den = den + ex[j];
                 }
+                if (!a.renorm) den = den_all;
                 for (int j = 0; j < k; ++j) {
                     a.topk_idx[t * k + j] = sel_e[j];
                     a.topk_w[t * k + j] = ex[j] / den;
@@ -604,6 +612,13 @@ __global__ void __launch_bounds__(kCThreads, S::MINB) route_cluster_kernel(Route
                 sel_e[j] = be;
                 sel_l[j] = bv;
             }
+            // without renormalisation the denominator runs over all E experts
+            float den_all = 0.0f;
+            if (!a.renorm) {
+                for (int uu = 0; lane + 32 * uu < E; ++uu) den_all += expf(l[lane + 32 * uu] - sel_l[0]);
+#pragma unroll
+                for (int st = 16; st >= 1; st >>= 1) den_all += __shfl_xor_sync(kFull, den_all, st);
+            }
             if (lane == 0) {
                 const float mx = sel_l[0];
                 float ex[8];
@@ -614,6 +629,7 @@ __global__ void __launch_bounds__(kCThreads, S::MINB) route_cluster_kernel(Route
                     ex[j] = expf(sel_l[j] - mx);
                     den = den + ex[j];
                 }
+                if (!a.renorm) den = den_all;
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     if (j >= k) break;
@@ -704,6 +720,41 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s)
     if (a.E <= 16) return launch_route_t<16, 2>(a, num_sms, s);
     if (a.E <= 32) return launch_route_t<32, 2>(a, num_sms, s);
     return launch_route_t<64, 1>(a, num_sms, s);
+}
+
+// The shared expert's sigmoid gate: one warp per token, fp32 dot product (the
+// lane sums and a butterfly; no integer depends on it), then 1/(1+exp(-d)).
+__global__ void shared_gate_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wsg,
+                                   float* __restrict__ scale, int64_t T, int32_t H)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+        float d = 0.0f;
+        for (int c = lane; c < H / 8; c += 32) {
+            const uint4 xv = __ldg(reinterpret_cast<const uint4*>(x + t * H + 8 * c));
+            const uint4 wv = __ldg(reinterpret_cast<const uint4*>(wsg + 8 * c));
+            const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                d = fmaf(bf16_lo(xw[u]), bf16_lo(ww[u]), d);
+                d = fmaf(bf16_hi(xw[u]), bf16_hi(ww[u]), d);
+            }
+        }
+#pragma unroll
+        for (int st = 16; st >= 1; st >>= 1) d += __shfl_xor_sync(0xffffffffu, d, st);
+        if (lane == 0) scale[t] = 1.0f / (1.0f + expf(-d));
+    }
+}
+
+cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* wsg, float* scale, int64_t T,
+                               int32_t H, int num_sms, cudaStream_t s)
+{
+    if (T == 0) return cudaSuccess;
+    const int64_t blocks_needed = (T + 7) / 8;
+    const int64_t cap = (int64_t)num_sms * 8;
+    shared_gate_kernel<<<(int)(blocks_needed < cap ? blocks_needed : cap), 256, 0, s>>>(x, wsg, scale, T, H);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -22,7 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 
 EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_set_option",
-           "moe_get_option", "moe_permute_static"]
+           "moe_get_option", "moe_permute_static", "moe_route_ex", "moe_layer_forward_ex"]
 
 OPT_GEMM0_A = 0
 GEMM0_A_PERMUTED = 0      # dispatch copies token rows to x_perm; GEMM0 loads dense tiles
@@ -48,6 +48,10 @@ class StageEvents(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("before_route", "before_permute", "before_gemm0",
                                                "before_gemm1", "before_shared", "before_combine",
                                                "after_combine")]
+
+
+class Gating(ctypes.Structure):
+    _fields_ = [("renormalize", ctypes.c_int32), ("shared_gate", ctypes.c_void_p)]
 
 
 class RoutingOut(ctypes.Structure):
@@ -91,6 +95,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_expert_ffn.argtypes = [D, P, P, P, P, P, P, P, P, P, sz, P]
     lib.moe_combine.restype = ctypes.c_int
     lib.moe_combine.argtypes = [D, P, i32, P, P]
+    lib.moe_route_ex.restype = ctypes.c_int
+    lib.moe_route_ex.argtypes = [D, P, P, P, ctypes.POINTER(Gating), P, P, P]
+    lib.moe_layer_forward_ex.restype = ctypes.c_int
+    lib.moe_layer_forward_ex.argtypes = [D, P, P, P, ctypes.POINTER(Gating), P, P, P, P, P, P, P,
+                                         ctypes.POINTER(RoutingOut), P, sz, ctypes.POINTER(StageEvents), P]
     lib.moe_layer_forward.restype = ctypes.c_int
     lib.moe_layer_forward.argtypes = [D, P, P, P, P, P, P, P, P, P, P, ctypes.POINTER(RoutingOut), P,
                                       sz, ctypes.POINTER(StageEvents), P]
@@ -151,13 +160,21 @@ def check(ws: torch.Tensor, stream=None) -> int:
     return int(load().moe_check(_p(ws), _stream(stream)))
 
 
-def route(dims: Dims, x, Wg, bias=None, topk_idx=None, topk_w=None, stream=None):
+def _gating(renormalize=True, shared_gate=None):
+    if renormalize and shared_gate is None:
+        return None
+    return Gating(1 if renormalize else 0, None if shared_gate is None else shared_gate.data_ptr())
+
+
+def route(dims: Dims, x, Wg, bias=None, topk_idx=None, topk_w=None, stream=None, renormalize=True):
     T, k = dims.T, dims.k
     dev = x.device
     topk_idx = topk_idx if topk_idx is not None else torch.empty(T, k, dtype=torch.int32, device=dev)
     topk_w = topk_w if topk_w is not None else torch.empty(T, k, dtype=torch.float32, device=dev)
-    _ok(load().moe_route(ctypes.byref(dims), _p(x), _p(Wg), _p(bias), _p(topk_idx), _p(topk_w),
-                         _stream(stream)), "moe_route")
+    g = _gating(renormalize)
+    _ok(load().moe_route_ex(ctypes.byref(dims), _p(x), _p(Wg), _p(bias),
+                            ctypes.byref(g) if g is not None else None, _p(topk_idx), _p(topk_w),
+                            _stream(stream)), "moe_route_ex")
     return topk_idx, topk_w
 
 
@@ -230,18 +247,26 @@ def routing_buffers(dims: Dims, device) -> Routing:
 
 def layer_forward(dims: Dims, x, Wg, W1, W3, W2, ws, bias=None, W1s=None, W3s=None, W2s=None,
                   out=None, routing: Routing | None = None, events: StageEvents | None = None,
-                  stream=None):
+                  stream=None, renormalize=True, shared_gate=None):
     if out is None:
         out = torch.empty(dims.T, dims.H, dtype=torch.bfloat16, device=x.device)
     r = None
     if routing is not None:
         r = RoutingOut(*(ctypes.c_void_p(getattr(routing, n).data_ptr()) for n in
                          ("topk_idx", "topk_w", "counts", "offsets", "src_row", "inv_pos")))
-    _ok(load().moe_layer_forward(ctypes.byref(dims), _p(x), _p(Wg), _p(bias), _p(W1), _p(W3), _p(W2),
-                                 _p(W1s), _p(W3s), _p(W2s), _p(out),
-                                 ctypes.byref(r) if r is not None else None, _p(ws), ws.numel(),
-                                 ctypes.byref(events) if events is not None else None,
-                                 _stream(stream)), "moe_layer_forward")
+    g = _gating(renormalize, shared_gate)
+    if g is None:
+        _ok(load().moe_layer_forward(ctypes.byref(dims), _p(x), _p(Wg), _p(bias), _p(W1), _p(W3), _p(W2),
+                                     _p(W1s), _p(W3s), _p(W2s), _p(out),
+                                     ctypes.byref(r) if r is not None else None, _p(ws), ws.numel(),
+                                     ctypes.byref(events) if events is not None else None,
+                                     _stream(stream)), "moe_layer_forward")
+    else:
+        _ok(load().moe_layer_forward_ex(ctypes.byref(dims), _p(x), _p(Wg), _p(bias), ctypes.byref(g),
+                                        _p(W1), _p(W3), _p(W2), _p(W1s), _p(W3s), _p(W2s), _p(out),
+                                        ctypes.byref(r) if r is not None else None, _p(ws), ws.numel(),
+                                        ctypes.byref(events) if events is not None else None,
+                                        _stream(stream)), "moe_layer_forward_ex")
     return out
 
 
