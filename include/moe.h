@@ -114,11 +114,14 @@ enum {
      *                          dispatch order (x_perm, in the workspace) and
      *                          GEMM0 loads dense 128-row TMA tiles;
      *   MOE_GEMM0_A_TMA_GATHER the GEMM0 producer warp gathers them straight
-     *                          from x with TMA gather4, 4 rows per instruction.
-     * Both give bit-identical results. */
+     *                          from x with TMA gather4, 4 rows per instruction;
+     *   MOE_GEMM0_A_CP_GATHER  a GEMM0 producer warp gathers them straight
+     *                          from x with 16-byte cp.async copies.
+     * All give bit-identical results. */
     MOE_OPT_GEMM0_A = 0,
     MOE_GEMM0_A_PERMUTED = 0,
     MOE_GEMM0_A_TMA_GATHER = 1,
+    MOE_GEMM0_A_CP_GATHER = 2,
     /* Where moe_layer_forward sums the k weighted expert rows of a token:
      *   MOE_COMBINE_AUTO     (default) fused when the last GEMM1 to run (the
      *                        shared expert's if any, else the routed one) has

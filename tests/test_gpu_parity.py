@@ -266,19 +266,18 @@ def test_zipf_bias_small(lib, oracle):
 GATHER_CASES = ["tiny", "ragged", "f_tail", "h_tail_e64", "shared", "one_token", "e256"]
 
 
-@pytest.fixture
-def tma_gather(lib):
-    """Runs the test with GEMM0 gathering its rows by TMA gather4."""
-    lib.set_gemm0_a(lib.GEMM0_A_TMA_GATHER)
-    yield
-    lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
-
-
+@pytest.mark.parametrize("path", ["tma_gather", "cp_gather"])
 @pytest.mark.parametrize("name", GATHER_CASES)
-def test_small_case_tma_gather(lib, oracle, tma_gather, name):
-    """The same edge cases with the TMA gather4 A path."""
-    T, H, F, E, k, Fs = SMALL_CASES[name]
-    run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=1, tol="elementwise")
+def test_small_case_gather_paths(lib, oracle, name, path):
+    """The same edge cases with GEMM0 gathering its rows itself (TMA gather4,
+    or cp.async by a producer warp)."""
+    default = lib.get_gemm0_a()
+    lib.set_gemm0_a(lib.GEMM0_A_TMA_GATHER if path == "tma_gather" else lib.GEMM0_A_CP_GATHER)
+    try:
+        T, H, F, E, k, Fs = SMALL_CASES[name]
+        run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=1, tol="elementwise")
+    finally:
+        lib.set_gemm0_a(default)
 
 
 @pytest.mark.parametrize("shape", [(300, 256, 192, 8, 2, 0), (257, 192, 128, 64, 6, 0),
@@ -324,16 +323,17 @@ def test_gather_paths_bit_identical(lib):
     dims = lib.make_dims(T, H, F, E, k, Fs)
     ws = lib.workspace(dims)
     outs = []
-    for mode in (lib.GEMM0_A_PERMUTED, lib.GEMM0_A_TMA_GATHER):
+    default = lib.get_gemm0_a()
+    for mode in (lib.GEMM0_A_PERMUTED, lib.GEMM0_A_TMA_GATHER, lib.GEMM0_A_CP_GATHER):
         lib.set_gemm0_a(mode)
         try:
             outs.append(lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws,
                                           W1s=g["W1s"], W3s=g["W3s"], W2s=g["W2s"]).clone())
         finally:
-            lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
+            lib.set_gemm0_a(default)
     torch.cuda.synchronize()
     assert lib.check(ws) == lib.MOE_OK
-    assert torch.equal(outs[0], outs[1])
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
 def test_deterministic(lib, oracle):

@@ -184,7 +184,8 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
                             const int32_t* tile_start, const int32_t* offsets, const uint16_t* W1,
                             const uint16_t* W3, const uint16_t* W2, const float* topk_w, float* slot,
                             uint16_t* h, uint32_t* err, int sms, cudaStream_t s, moe_event_t ev_mid,
-                            const FusedCombine& fc = FusedCombine{false, 0, 0, nullptr, nullptr})
+                            const FusedCombine& fc = FusedCombine{false, 0, 0, nullptr, nullptr},
+                            bool cp_gather = false)
 {
     if (M == 0) {
         if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
@@ -213,7 +214,9 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
     a.N = F;
     a.K = d.H;
     a.h_out = reinterpret_cast<__nv_bfloat16*>(h);
-    MOE_TRY(launch_grouped_gemm(dense ? kGemm0Dense : kGemm0Gather, mx, m1, m3, a, sms, s));
+    a.x = x;
+    MOE_TRY(launch_grouped_gemm(dense ? kGemm0Dense : cp_gather ? kGemm0CpGather : kGemm0Gather, mx, m1,
+                                m3, a, sms, s));
     if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
     // GEMM1 + weighted scatter: h [rows, F] x W2 [F, H] -> slot[rank][token]
     a.N = d.H;
@@ -260,7 +263,9 @@ const char* moe_status_string(int status)
 moe_status moe_set_option(int option, int value)
 {
     if (option == MOE_OPT_GEMM0_A) {
-        if (value != MOE_GEMM0_A_PERMUTED && value != MOE_GEMM0_A_TMA_GATHER) return MOE_ERR_INVALID_ARG;
+        if (value != MOE_GEMM0_A_PERMUTED && value != MOE_GEMM0_A_TMA_GATHER &&
+            value != MOE_GEMM0_A_CP_GATHER)
+            return MOE_ERR_INVALID_ARG;
         g_gemm0_a.store(value);
         return MOE_OK;
     }
@@ -370,7 +375,10 @@ moe_status moe_expert_ffn(const moe_dims* dims, const moe_bf16* x, const int32_t
     }
     const int32_t R = (int32_t)(dims->T * dims->k);
     const uint16_t* x_rows = nullptr;
-    if (g_gemm0_a.load() == MOE_GEMM0_A_PERMUTED) {
+    const int a_opt = g_gemm0_a.load();
+    if (a_opt == MOE_GEMM0_A_CP_GATHER && !src_row && dims->k == 1) {
+        x_rows = x;   // identity dispatch: x is already in dispatch order
+    } else if (a_opt == MOE_GEMM0_A_PERMUTED) {
         if (!src_row && dims->k == 1) {
             x_rows = x;   // identity dispatch: x is already in dispatch order
         } else {
@@ -383,7 +391,8 @@ moe_status moe_expert_ffn(const moe_dims* dims, const moe_bf16* x, const int32_t
     MOE_TRY_STATUS(run_expert_gemms(*dims, R, dims->F, dims->E, dims->k, x, x_rows, src_row, tile,
                                     offsets, W1, W3, W2, topk_w, slot,
                                     reinterpret_cast<uint16_t*>(bytes(ws) + L.h), err, sms, s,
-                                    nullptr));
+                                    nullptr, FusedCombine{false, 0, 0, nullptr, nullptr},
+                                    a_opt == MOE_GEMM0_A_CP_GATHER));
     return finish(cudaSuccess, ws, s);
 }
 
@@ -468,7 +477,9 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                    R, d.E};
     MOE_TRY(launch_permute(pa, s));
 
-    const bool permuted = (g_gemm0_a.load() == MOE_GEMM0_A_PERMUTED);
+    const int a_opt = g_gemm0_a.load();
+    const bool permuted = (a_opt == MOE_GEMM0_A_PERMUTED);
+    const bool cp_gather = (a_opt == MOE_GEMM0_A_CP_GATHER);
     uint16_t* xp = reinterpret_cast<uint16_t*>(w + L.xp);
     if (permuted)
         MOE_TRY(launch_gather_rows(x, src, offsets + d.E, xp, R, d.T, d.H, d.k, err, sms, s));
@@ -478,7 +489,7 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                                     tile, offsets, W1, W3, W2, tw, slot,
                                     reinterpret_cast<uint16_t*>(w + L.h), err, sms, s,
                                     events ? events->before_gemm1 : nullptr,
-                                    FusedCombine{fused, 0, n_slots, arrive, out}));
+                                    FusedCombine{fused, 0, n_slots, arrive, out}, cp_gather));
 
     record(events ? events->before_shared : nullptr, s);
     if (d.F_shared > 0) {
@@ -489,7 +500,8 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
             MOE_TRY(launch_shared_gate(x, shared_gate, sgate, d.T, d.H, sms, s));
         }
         // identity dispatch: every token, in token order, weight 1
-        MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)d.T, d.F_shared, 1, 1, x, permuted ? x : nullptr,
+        MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)d.T, d.F_shared, 1, 1, x,
+                                        (permuted || cp_gather) ? x : nullptr,
                                         nullptr, nullptr, nullptr, W1s, W3s, W2s, sgate,
                                         fused ? slot : slot + (size_t)d.k * d.T * d.H,
                                         reinterpret_cast<uint16_t*>(w + L.hs), err, sms, s, nullptr,

@@ -14,10 +14,16 @@
 //                      step (an HBM-bound copy);
 //       kGemm0Gather - the producer warp gathers the rows of x itself with
 //                      TMA gather4 (4 rows per instruction, indices from
-//                      src_row), so no permuted copy of x is written. On GB300
-//                      32 gather4 per 16 KB stage cannot keep up with the
-//                      tensor cores (measured: ~0.5 vs ~1.7 PFLOP/s for the
-//                      Mixtral-shaped GEMM0), so the dense form is the default.
+//                      src_row), so no permuted copy of x is written;
+//       kGemm0CpGather - a second producer warp gathers the rows with 16-byte
+//                      cp.async copies straight into the 128-byte-swizzled
+//                      tile (32 per lane per stage), waits for them two stages
+//                      later, fences them into the async proxy and only then
+//                      arrives on the stage's barrier (which also counts the
+//                      TMA bytes of B). No x_perm round trip through HBM.
+//     Both gather forms measured ~0.5 PFLOP/s on GB300 against ~1.7 for the
+//     dense form: 128 scattered 128-byte rows per stage do not arrive fast
+//     enough for one CTA, whatever issues them. kGemm0Dense is the default.
 //     B is [W1 | W3] for one 128-wide slice of F: one 128x256 MMA tile gives
 //     both x W1 and x W3, and the epilogue writes h = silu(x W1) * (x W3) in
 //     bf16.
@@ -63,7 +69,8 @@ constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int B_BYTES = BN * BK * 2;         // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int B_CHUNK_BYTES = BK * 128;      // one 64-column slice of B: 64 k-rows x 128 B
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 224;   // 7 warps: TMA, MMA, 4 x epilogue, row gather
+constexpr int GATHER_LAG = 2;      // stages a gathered A tile is given to land
 constexpr int MAX_GROUPS = 257;
 constexpr int TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
@@ -78,6 +85,7 @@ struct SmemTail {
     int abort;
     int tile_start[MAX_GROUPS + 1];
     int offsets[MAX_GROUPS + 1];
+    int tok[BM];                      // kGemm0CpGather: token of each row of the current tile
 };
 
 constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(SmemTail);
@@ -116,7 +124,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     unsigned char* tiles = smem_raw + (tiles_addr - raw_addr);
     SmemTail* st = reinterpret_cast<SmemTail*>(tiles + (size_t)STAGES * STAGE_BYTES);
 
-    constexpr bool IS_GEMM0 = (MODE == kGemm0Gather || MODE == kGemm0Dense);
+    constexpr bool IS_GEMM0 = (MODE == kGemm0Gather || MODE == kGemm0Dense || MODE == kGemm0CpGather);
+    constexpr bool CP_GATHER = (MODE == kGemm0CpGather);
     constexpr bool GATHER = (MODE == kGemm0Gather);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -125,7 +134,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // ---- set-up
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&st->full[s]), 1);
+            // with cp.async rows, a stage is full after the TMA bytes of B and
+            // the gather warp's arrival
+            mbar_init(smem_u32(&st->full[s]), CP_GATHER ? 2 : 1);
             mbar_init(smem_u32(&st->empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -202,11 +213,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint32_t full = smem_u32(&st->full[stage]);
                 const uint32_t a_dst = tiles_addr + stage * STAGE_BYTES;
                 const uint32_t b_dst = a_dst + A_BYTES;
-                if (lane == 0) mbar_arrive_expect_tx(full, STAGE_BYTES);
+                if (lane == 0) mbar_arrive_expect_tx(full, CP_GATHER ? B_BYTES : STAGE_BYTES);
                 __syncwarp();
                 if (GATHER)
                     tma_gather4(a_dst + lane * 512, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], full);
-                else if (lane == 0)
+                else if (!CP_GATHER && lane == 0)
                     tma_load_2d(a_dst, &tmA, kb * BK, wk.row0, full);
                 if (IS_GEMM0) {
                     if (lane == 0) {
@@ -283,6 +294,67 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
         }
         __syncwarp();
+    } else if (warp == 6) {
+        // ========================= A row gather (cp.async) ======================
+        if (CP_GATHER) {
+            int stage = 0, done_stage = 0;
+            uint32_t phase = 0;
+            int pending = 0;   // stages issued whose rows are not yet published
+            bool ok = true;
+            const int c = lane & 7;        // 16-byte chunk of a 128-byte row
+            const int rsub = lane >> 3;    // row within a group of four
+            auto publish_oldest = [&]() {
+                // the oldest pending stage's copies have landed (this lane's): make
+                // them visible to the tensor cores, then arrive once for the warp
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&st->full[done_stage]));
+                if (++done_stage == STAGES) done_stage = 0;
+                --pending;
+            };
+            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const Work wk = decode_work(w, n_tiles, st->tile_start, st->offsets, G);
+                __syncwarp();   // the previous tile's rows are no longer read
+                for (int rr = lane; rr < BM; rr += 32) {
+                    const int p = wk.row0 + min(rr, wk.rows - 1);
+                    const int f = args.src_row ? args.src_row[p] : p;
+                    int t = f / args.k;
+                    if (f < 0 || t >= args.T) {
+                        report_error(args.err, MOE_DEV_ERR_BOUNDS);
+                        t = 0;
+                    }
+                    st->tok[rr] = t;
+                }
+                __syncwarp();
+                for (int kb = 0; kb < k_blocks; ++kb) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(smem_u32(&st->empty[stage]), phase ^ 1u, abort, args.err))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a_dst = tiles_addr + stage * STAGE_BYTES;
+                    const uint16_t* xk = args.x + kb * BK + c * 8;
+#pragma unroll 8
+                    for (int q = 0; q < BM / 4; ++q) {
+                        const int r = 4 * q + rsub;
+                        const uint16_t* src = xk + (int64_t)st->tok[r] * args.K;
+                        const uint32_t dst = a_dst + r * 128 + ((c ^ (r & 7)) << 4);
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src)
+                                     : "memory");
+                    }
+                    asm volatile("cp.async.commit_group;" ::: "memory");
+                    ++pending;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    if (pending > GATHER_LAG) {
+                        asm volatile("cp.async.wait_group %0;" ::"n"(GATHER_LAG) : "memory");
+                        publish_oldest();
+                    }
+                }
+            }
+            // the last stages (and, after an abort, whatever is in flight)
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+            while (pending > 0) publish_oldest();
+        }
     } else {
         // ============================== epilogue ==============================
         const int ew = warp & 3;               // TMEM lane quarter this warp may access
@@ -441,6 +513,7 @@ cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensor
     else if (mode == kGemm0Dense) kern = grouped_gemm_kernel<kGemm0Dense>;
     else if (mode == kGemm1Scatter) kern = grouped_gemm_kernel<kGemm1Scatter>;
     else if (mode == kGemm1Combine) kern = grouped_gemm_kernel<kGemm1Combine>;
+    else if (mode == kGemm0CpGather) kern = grouped_gemm_kernel<kGemm0CpGather>;
     else return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;

@@ -56,7 +56,10 @@ cudaError_t launch_tile_table(const int32_t* offsets, int32_t G, int32_t* tile_s
 // from the dispatch-ordered copy x_perm (kGemm0Dense); GEMM1 + weighted scatter
 // (kGemm1Scatter), or GEMM1 + weighted scatter + the combine done by the last
 // of the n_slots contributions to each (token, 256-column tile) (kGemm1Combine).
-enum GemmMode { kGemm0Gather = 0, kGemm1Scatter = 1, kGemm0Dense = 2, kGemm1Combine = 3 };
+// kGemm0CpGather: GEMM0 whose A rows are gathered from x by a producer warp
+// with 16-byte cp.async copies (no x_perm).
+enum GemmMode { kGemm0Gather = 0, kGemm1Scatter = 1, kGemm0Dense = 2, kGemm1Combine = 3,
+                kGemm0CpGather = 4 };
 
 struct GemmArgs {
     int32_t M;                   // rows in dispatched order (R, or T for a dense expert)
@@ -70,6 +73,7 @@ struct GemmArgs {
     const int32_t* src_row;      // [M] or null (identity)
     const float* topk_w;         // GEMM1: [M] by f, or null (weight 1)
     __nv_bfloat16* h_out;        // GEMM0: [M, N]
+    const uint16_t* x;           // kGemm0CpGather: x [T, K] (A rows gathered by token)
     float* slot;                 // GEMM1: slot array [n_slots, T, N]; rank j goes to slot_j0 + j
     int32_t slot_j0;             // GEMM1: first slot of this launch (the shared expert: k)
     int32_t n_slots;             // kGemm1Combine: contributions summed per (token, N tile)
@@ -78,7 +82,8 @@ struct GemmArgs {
     uint32_t* err;
 };
 
-// tmA: kGemm0Gather -> x [T,H] (box 64 x 1, gathered); kGemm0Dense -> x_perm
+// tmA: kGemm0CpGather -> unused (A comes from args.x);
+//      kGemm0Gather -> x [T,H] (box 64 x 1, gathered); kGemm0Dense -> x_perm
 // [M,H] (box 64 x 128); kGemm1Scatter -> h [M,F] (box 64 x 128).
 // tmB0/tmB1: GEMM0 -> W1 / W3 viewed as [G*H, F]; GEMM1 -> W2 viewed as [G*F, H]
 // (tmB1 unused). All boxes 64 wide with 128-byte swizzle.

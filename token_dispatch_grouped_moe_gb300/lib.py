@@ -27,6 +27,7 @@ EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check"
 OPT_GEMM0_A = 0
 GEMM0_A_PERMUTED = 0      # dispatch copies token rows to x_perm; GEMM0 loads dense tiles
 GEMM0_A_TMA_GATHER = 1    # GEMM0 producer gathers token rows with TMA gather4
+GEMM0_A_CP_GATHER = 2     # a GEMM0 producer warp gathers token rows with cp.async
 OPT_COMBINE = 1
 COMBINE_AUTO = 0          # fused when the last GEMM1 has K >= 4096
 COMBINE_FUSED = 1         # GEMM1's epilogue: the last contribution sums the slots
