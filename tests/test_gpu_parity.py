@@ -181,7 +181,7 @@ ORDER_CASES = [
 ]
 
 
-@pytest.mark.parametrize("E", [2, 16, 32, 64, 200])
+@pytest.mark.parametrize("E", [2, 8, 16, 32, 64, 200])
 @pytest.mark.parametrize("case", range(len(ORDER_CASES)))
 def test_route_canonical_order(lib, E, case):
     """The router's logits follow the canonical order bit for bit: expert 0's
@@ -218,6 +218,40 @@ def test_route_bias_added_after_sum(lib):
     idx, _ = lib.route(dims, x.bfloat16().cuda(), Wg.bfloat16().cuda(), bias=bias.cuda())
     torch.cuda.synchronize()
     assert idx.cpu().tolist()[0] == [0, 1]
+
+
+ROUTE_ONLY_CASES = [
+    # (T, H, E, k): more token groups than warps on the GPU (several per warp),
+    # a ragged last group, a hidden size that leaves a step partly padded
+    (6001, 512, 8, 2),
+    (5003, 320, 8, 3),
+    (4999, 256, 6, 2),
+    (9000, 128, 3, 1),
+]
+
+
+@pytest.mark.parametrize("biased", [False, True])
+@pytest.mark.parametrize("renormalize", [True, False])
+@pytest.mark.parametrize("case", ROUTE_ONLY_CASES)
+def test_route_only(lib, oracle, case, biased, renormalize):
+    """moe_route alone against the oracle: ids bit-exact, weights to 1e-5."""
+    T, H, E, k = case
+    inp = make_inputs(T, H, 64, E, seed=5)
+    b = {n: bf16_bits(v) for n, v in inp.items()}
+    bias = None
+    if biased:
+        bias = (np.random.default_rng(7).standard_normal(E) * 0.3).astype(np.float32)
+    dims = lib.make_dims(T, H, 64, E, k)
+    idx, w = lib.route(dims, inp["x"].cuda(), inp["Wg"].cuda(),
+                       bias=None if bias is None else torch.from_numpy(bias).cuda(),
+                       renormalize=renormalize)
+    torch.cuda.synchronize()
+    logits, ridx, rw = oracle.route(b["x"], b["Wg"], k, bias)
+    if not renormalize:
+        rw = oracle.gate_weights_full(logits, ridx)
+    assert np.array_equal(idx.cpu().numpy(), ridx), "top-k ids differ"
+    gw = w.cpu().numpy()
+    assert np.allclose(gw, rw, rtol=TOL_W, atol=1e-7), f"gate weights differ: {np.max(np.abs(gw - rw))}"
 
 
 def _wsg(H, seed):

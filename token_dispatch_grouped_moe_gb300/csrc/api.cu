@@ -68,20 +68,31 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2D bf16 tensor [outer, inner] (inner contiguous), box {64, box_outer},
-// 128-byte swizzle; out-of-bounds elements read as zero.
-bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer)
+}  // namespace
+
+bool encode_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                   uint32_t box_outer, bool swizzle_128)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * 2};
-    cuuint32_t box[2] = {64, box_outer};
+    cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    swizzle_128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+// 2D bf16 tensor [outer, inner] (inner contiguous), box {64, box_outer},
+// 128-byte swizzle; out-of-bounds elements read as zero.
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer)
+{
+    return encode_map_2d(m, base, inner, outer, 64, box_outer, true);
 }
 
 // ------------------------------------------------------------ workspace --
@@ -470,6 +481,7 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     record(events ? events->before_route : nullptr, s);
     RouteArgs ra{x, Wg, bias, idx, tw, d.T, d.H, d.E, d.k};
     ra.renorm = gating ? (gating->renormalize != 0) : 1;
+    ra.err = err;
     MOE_TRY(launch_route(ra, sms, s));
 
     record(events ? events->before_permute : nullptr, s);

@@ -21,8 +21,15 @@ struct RouteArgs {
     int64_t T;
     int32_t H, E, k;
     int32_t renorm = 1;    // 1: softmax over the k selected; 0: over all E
+    uint32_t* err = nullptr;   // device error word (a bounded wait that ran out), or null
 };
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s);
+
+// A TMA tensor map of a row-major bf16 matrix [outer, inner] with box
+// {box_inner, box_outer}, 128-byte swizzle or none; out-of-bounds elements
+// read as zero. False if the driver entry point or the encoding fails.
+bool encode_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
+                   uint32_t box_outer, bool swizzle_128);
 
 // scale[t] = 1 / (1 + exp(-x[t] . wsg)) (the shared expert's sigmoid gate)
 cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* wsg, float* scale, int64_t T,

@@ -12,7 +12,10 @@
 // lane sums are combined with an xor butterfly (strides 16, 8, 4, 2, 1).
 // That is bit for bit the order the oracle restates.
 //
-// Two kernels compute this order.
+// Three kernels compute this order.
+//
+// route_stream_kernel (E <= 8, the gate fits shared memory): see its own
+// comment below; TMA-fed per-warp pipelines and mixed-precision FMAs.
 //
 // route_cluster_kernel (8 < E <= 64). The canonical lanes are
 // independent until the butterfly, and lanes L and L' with L = L' (mod CS)
@@ -31,15 +34,16 @@
 // NT tokens x EW experts of fp32 accumulators; the warps of a CTA are split
 // into expert and token subgroups.
 //
-// route_kernel (E <= 8, E > 64, or a gate too large for a cluster of 8): one
-// CTA per SM, warp lane L = canonical lane L, the gate staged in 64 KB slices
-// of H for every group of tokens.
+// route_kernel (E > 64, or a gate too large for the other two): one CTA per
+// SM, warp lane L = canonical lane L, the gate staged in 64 KB slices of H for
+// every group of tokens.
 //
-// Both stage Wg in a lane-major layout, [step m][element i][expert octet q]
+// The last two stage Wg in a lane-major layout, [step m][element i][expert octet q]
 // [lane] of uint4 (8 bf16 experts), so the lanes of a warp read consecutive
 // 16-byte words (no bank conflicts).
 #include <cooperative_groups.h>
 #include <cstdint>
+#include <cstring>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -697,6 +701,300 @@ cudaError_t launch_cluster_any(const RouteArgs& a, int num_sms, cudaStream_t s, 
     return cudaSuccess;
 }
 
+
+// ----------------------------------------------------- streaming router --
+//
+// route_stream_kernel (E <= 8). One CTA per SM; every warp is an independent
+// pipeline over groups of NT tokens, so no CTA barrier couples the warps once
+// they run. Lane L of a warp is the canonical lane L.
+//
+// Gate. Kept bf16 in shared memory as the gate viewed as a [H/8][64] matrix
+// (row c = the 8 hidden rows of chunk c, 8 experts each) in 128-byte-swizzled
+// rows: chunk c's element i sits at byte c*128 + ((i ^ (c & 7)) << 4). The
+// 32 lanes of a warp read 32 consecutive chunks at one element, which the
+// swizzle spreads over all banks. With E == 8 the gate arrives by one TMA
+// copy per 256-element step, each completing its own mbarrier, so a warp
+// starts on step 0 while later steps are still in flight; otherwise (E < 8,
+// rows are not 16 bytes) threads stage it with plain stores.
+//
+// x. Each warp streams its tokens through a ring of D steps in shared memory,
+// one TMA copy (NT token rows x 256 elements) per step, D-1 steps ahead of
+// use. Bulk copies keep enough bytes in flight per SM to cover HBM latency,
+// which per-thread copies, limited by the outstanding-miss tracking of the
+// load path, did not (measured).
+//
+// FMAs. The mixed-precision form fma.rn.f32.bf16 takes the bf16 operands as
+// they are: widening bf16 to fp32 is exact and the product is rounded once
+// with the add, so each step is fmaf on the widened values, bit for bit, in
+// the canonical order. After a group's steps a transpose-reduce (the
+// butterfly's operands and tree) leaves every logit on one lane (two with
+// NT == 8), and the top-k runs as a shuffle argmax among the lanes that hold
+// one token's logits.
+
+// acc[e] = fma(x, g[e], acc[e]) for the 8 experts of one hidden element: x is
+// half XH of the x word, g[e] half e&1 of gate word e>>1.
+#define MOE_FMA8_BF16(XH)                                                                    \
+    asm("{\n\t.reg .b16 xl, xh, g0, g1, g2, g3, g4, g5, g6, g7;\n\t"                        \
+        "mov.b32 {xl, xh}, %8;\n\t"                                                            \
+        "mov.b32 {g0, g1}, %9;\n\t"                                                            \
+        "mov.b32 {g2, g3}, %10;\n\t"                                                           \
+        "mov.b32 {g4, g5}, %11;\n\t"                                                           \
+        "mov.b32 {g6, g7}, %12;\n\t"                                                           \
+        "fma.rn.f32.bf16 %0, " XH ", g0, %0;\n\t"                                              \
+        "fma.rn.f32.bf16 %1, " XH ", g1, %1;\n\t"                                              \
+        "fma.rn.f32.bf16 %2, " XH ", g2, %2;\n\t"                                              \
+        "fma.rn.f32.bf16 %3, " XH ", g3, %3;\n\t"                                              \
+        "fma.rn.f32.bf16 %4, " XH ", g4, %4;\n\t"                                              \
+        "fma.rn.f32.bf16 %5, " XH ", g5, %5;\n\t"                                              \
+        "fma.rn.f32.bf16 %6, " XH ", g6, %6;\n\t"                                              \
+        "fma.rn.f32.bf16 %7, " XH ", g7, %7;\n\t}"                                             \
+        : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3]), "+f"(acc[4]), "+f"(acc[5]),    \
+          "+f"(acc[6]), "+f"(acc[7])                                                             \
+        : "r"(xw), "r"(g.x), "r"(g.y), "r"(g.z), "r"(g.w))
+template <int HALF>
+__device__ __forceinline__ void fma8_bf16(float (&acc)[8], uint32_t xw, const uint4& g)
+{
+    if constexpr (HALF) MOE_FMA8_BF16("xh");
+    else MOE_FMA8_BF16("xl");
+}
+#undef MOE_FMA8_BF16
+
+template <int NT_, int D_, int NW_>
+struct SShape {
+    static constexpr int NT = NT_;   // tokens per warp group (rows of one x copy)
+    static constexpr int D = D_;     // x ring depth per warp, in steps
+    static constexpr int NW = NW_;   // warps per CTA
+    static constexpr int THREADS = NW * 32;
+    static constexpr int SLOT_BYTES = NT * 512;   // NT rows x 256 bf16
+    static size_t smem_bytes(int H)
+    {
+        const size_t n_steps = (size_t)(H / 8 + 31) / 32;
+        return 1024 + n_steps * 4096 + (size_t)NW * D * SLOT_BYTES + (n_steps + (size_t)NW * D) * 8 + 16;
+    }
+};
+
+template <class S>
+__global__ void __launch_bounds__(S::THREADS, 1)
+    route_stream_kernel(const __grid_constant__ CUtensorMap gmap, const __grid_constant__ CUtensorMap xmap,
+                        RouteArgs a, int gate_tma)
+{
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    constexpr int NT = S::NT, D = S::D, NW = S::NW;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int H = a.H, E = a.E, k = a.k;
+    const int n_steps = (H / 8 + 31) / 32;
+
+    unsigned char* gate = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);   // [m][32][128 B]
+    unsigned char* ring_all = gate + (size_t)n_steps * 4096;
+    unsigned char* ring = ring_all + (size_t)warp * D * S::SLOT_BYTES;               // [slot][token][512 B]
+    uint64_t* gbar = reinterpret_cast<uint64_t*>(ring_all + (size_t)NW * D * S::SLOT_BYTES);
+    uint64_t* xbar = gbar + n_steps + warp * D;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbar + n_steps + NW * D);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        if (gate_tma)
+            for (int m = 0; m < n_steps; ++m) mbar_init(smem_u32(gbar + m), 1);
+        for (int b = 0; b < NW * D; ++b) mbar_init(smem_u32(gbar + n_steps + b), 1);
+        fence_barrier_init();
+    }
+    if (!gate_tma) {
+        for (int h = threadIdx.x; h < n_steps * 256; h += S::THREADS) {
+            uint32_t w[4] = {0, 0, 0, 0};
+            if (h < H)
+                for (int e = 0; e < E; ++e)
+                    w[e >> 1] |= (uint32_t)a.Wg[(int64_t)h * E + e] << (16 * (e & 1));
+            const int c = h >> 3, i = h & 7;
+            *reinterpret_cast<uint4*>(gate + (size_t)c * 128 + ((i ^ (c & 7)) << 4)) =
+                make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+    __syncthreads();   // barriers initialised (and a plainly staged gate visible)
+    if (gate_tma && threadIdx.x == 0) {
+        for (int m = 0; m < n_steps; ++m) {
+            mbar_arrive_expect_tx(smem_u32(gbar + m), 4096);
+            tma_load_2d(smem_u32(gate + (size_t)m * 4096), &gmap, 0, 32 * m, smem_u32(gbar + m));
+        }
+    }
+
+    // token groups: warp w of CTA b takes g = b + grid * (w + NW * j), j = 0, 1, ..
+    const int64_t G = (a.T + NT - 1) / NT;
+    const int64_t g_first = blockIdx.x + (int64_t)gridDim.x * warp;
+    const int64_t g_stride = (int64_t)gridDim.x * NW;
+
+    // prefetch cursor, D-1 steps ahead; lane 0 issues the copies
+    int64_t pf_g = g_first;
+    int pf_m = 0, pf_slot = 0;
+    auto pf_issue = [&]() {
+        if (pf_g < G) {
+            if (lane == 0) {
+                // the slot was last read a step ago (the __syncwarp before
+                // this call): order those reads before the async-proxy write
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const uint32_t bar = smem_u32(xbar + pf_slot);
+                mbar_arrive_expect_tx(bar, S::SLOT_BYTES);
+                tma_load_2d(smem_u32(ring + (size_t)pf_slot * S::SLOT_BYTES), &xmap, 256 * pf_m,
+                            (int32_t)(pf_g * NT), bar);
+            }
+            if (++pf_m == n_steps) { pf_m = 0; pf_g += g_stride; }
+            if (++pf_slot == D) pf_slot = 0;
+        }
+    };
+#pragma unroll
+    for (int j = 0; j < D - 1; ++j) pf_issue();
+
+    // this lane's gate words: chunk 32m + lane, element i at gl + m*4096 + (i ^ (lane & 7))*16
+    const unsigned char* gl = gate + lane * 128;
+    const int sw = lane & 7;
+
+    // the lanes that hold one token's logits after the reduce
+    constexpr int NV = NT * 8 > 32 ? NT * 8 / 32 : 1;       // logits per lane
+    constexpr int LOG_DUP = NT == 1 ? 2 : NT == 2 ? 1 : 0;   // lanes holding copies
+    constexpr int SL = 32 / NT;                              // lanes per token
+    static_assert(NT == 1 || NT == 2 || NT == 4 || NT == 8, "NT in {1, 2, 4, 8}");
+    const int vbase = NV * (lane >> LOG_DUP);
+    const int my_tt = vbase >> 3;
+    const int e0 = vbase & 7;
+
+    int cur = 0;
+    uint32_t phases = 0;   // bit s: parity of the next completion of slot s
+    bool first = true;
+    for (int64_t g = g_first; g < G; g += g_stride) {
+        float acc[NT][8];
+#pragma unroll
+        for (int tt = 0; tt < NT; ++tt)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[tt][e] = 0.0f;
+
+        for (int m = 0; m < n_steps; ++m) {
+            __syncwarp();   // every lane is done with the slot the next copy overwrites
+            pf_issue();
+            if (gate_tma && first) mbar_wait(smem_u32(gbar + m), 0, abort_flag, a.err);
+            mbar_wait(smem_u32(xbar + cur), (phases >> cur) & 1u, abort_flag, a.err);
+            phases ^= 1u << cur;
+            const unsigned char* xs = ring + (size_t)cur * S::SLOT_BYTES + lane * 16;
+            uint4 xv[NT];
+#pragma unroll
+            for (int tt = 0; tt < NT; ++tt) xv[tt] = *reinterpret_cast<const uint4*>(xs + tt * 512);
+            const unsigned char* gs = gl + (size_t)m * 4096;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {   // elements 2q, 2q+1: word q of each x chunk
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const uint4 gw = *reinterpret_cast<const uint4*>(gs + (((2 * q + half) ^ sw) << 4));
+#pragma unroll
+                    for (int tt = 0; tt < NT; ++tt) {
+                        const uint32_t w = q == 0 ? xv[tt].x : q == 1 ? xv[tt].y : q == 2 ? xv[tt].z : xv[tt].w;
+                        if (half) fma8_bf16<1>(acc[tt], w, gw);
+                        else fma8_bf16<0>(acc[tt], w, gw);
+                    }
+                }
+            }
+            if (++cur == D) cur = 0;
+        }
+        first = false;
+
+        // the butterfly over the 32 canonical lanes, as a transpose-reduce:
+        // afterwards this lane holds logits e0 .. e0+NV-1 of token my_tt
+        float v[NT * 8];
+#pragma unroll
+        for (int tt = 0; tt < NT; ++tt)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[tt * 8 + e] = acc[tt][e];
+        transpose_reduce<NT * 8, 16>(v, lane);
+        float l[NV];
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            l[u] = v[u];
+            if (a.bias && e0 + u < E) l[u] = l[u] + a.bias[e0 + u];
+        }
+
+        // top-k: k rounds of an argmax over the token's lanes (larger logit,
+        // ties to the lower id); the winner's holder marks it taken
+        uint32_t taken = 0;
+        int sel_e[8];
+        float sel_l[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j >= k) break;
+            float bv = 0.0f;
+            int be = -1;
+#pragma unroll
+            for (int u = 0; u < NV; ++u) {
+                const bool ok = (e0 + u < E) && !((taken >> u) & 1u);
+                if (ok && (be < 0 || l[u] > bv)) { bv = l[u]; be = e0 + u; }
+            }
+#pragma unroll
+            for (int st = 1; st < SL; st <<= 1) {
+                const float ov = __shfl_xor_sync(kFull, bv, st);
+                const int oe = __shfl_xor_sync(kFull, be, st);
+                const bool better = (oe >= 0) && (be < 0 || ov > bv || (ov == bv && oe < be));
+                if (better) { bv = ov; be = oe; }
+            }
+            if (be >= e0 && be < e0 + NV) taken |= 1u << (be - e0);
+            sel_e[j] = be;
+            sel_l[j] = bv;
+        }
+        const float mx = sel_l[0];
+        // without renormalisation the denominator runs over all E experts
+        float den_all = 0.0f;
+        if (!a.renorm) {
+#pragma unroll
+            for (int u = 0; u < NV; ++u)
+                if (e0 + u < E && (lane & ((1 << LOG_DUP) - 1)) == 0) den_all = den_all + expf(l[u] - mx);
+#pragma unroll
+            for (int st = 1; st < SL; st <<= 1) den_all = den_all + __shfl_xor_sync(kFull, den_all, st);
+        }
+        const int64_t t = g * NT + my_tt;
+        if ((lane & (SL - 1)) == 0 && t < a.T) {
+            float ex[8];
+            float den = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= k) break;
+                ex[j] = expf(sel_l[j] - mx);
+                den = den + ex[j];
+            }
+            if (!a.renorm) den = den_all;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= k) break;
+                a.topk_idx[t * k + j] = sel_e[j];
+                a.topk_w[t * k + j] = ex[j] / den;
+            }
+        }
+    }
+    // every x copy a warp issued, it also waited for; a warp without tokens
+    // never waited on the gate: no CTA exits while its copies may still land
+    if (gate_tma && threadIdx.x == 0)
+        for (int m = 0; m < n_steps; ++m) mbar_wait_drain(smem_u32(gbar + m), 0);
+}
+
+// Returns false (nothing launched) when a tensor map cannot be made.
+template <class S>
+bool launch_stream(const RouteArgs& a, int num_sms, cudaStream_t s, cudaError_t& err)
+{
+    CUtensorMap gmap, xmap;
+    std::memset(&gmap, 0, sizeof(gmap));
+    // x as a bf16 [T, H] matrix, box {256, NT}: one step of NT token rows
+    if (!encode_map_2d(&xmap, a.x, (uint64_t)a.H, (uint64_t)a.T, 256, S::NT, false)) return false;
+    // the gate Wg[H, 8] as a bf16 [H/8, 64] matrix, box {64, 32}, 128-byte swizzle
+    const bool gate_tma = a.E == 8 && encode_map_2d(&gmap, a.Wg, 64, (uint64_t)a.H / 8, 64, 32, true);
+    const size_t smem = S::smem_bytes(a.H);
+    auto kern = route_stream_kernel<S>;
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return true;
+    // one CTA per SM while there are groups for each: the groups are dealt
+    // round-robin over the CTAs first, so every SM gets within one of the same
+    // number of groups
+    const int64_t G = (a.T + S::NT - 1) / S::NT;
+    const int grid = (int)(G < num_sms ? G : num_sms);
+    kern<<<grid, S::THREADS, smem, s>>>(gmap, xmap, a, gate_tma ? 1 : 0);
+    err = cudaGetLastError();
+    return true;
+}
+
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s)
@@ -704,11 +1002,12 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s)
     if (a.T == 0) return cudaSuccess;
     bool launched = false;
     cudaError_t err = cudaSuccess;
-    // E <= 8: the whole gate fits one CTA; route_kernel measured faster there
-    // (38.8 vs 44.0 us for 8192 x 4096, E = 8).
-    if (a.E <= 8)
-        launched = false;
-    else if (a.E <= 16)
+    // E <= 8: the streaming router while its gate fits shared memory
+    constexpr size_t kStreamBudget = 227 * 1024;
+    if (a.E <= 8) {
+        if (SShape<8, 4, 8>::smem_bytes(a.H) <= kStreamBudget && launch_stream<SShape<8, 4, 8>>(a, num_sms, s, err))
+            return err;
+    } else if (a.E <= 16)
         err = launch_cluster_any<16, 1, 2, 1, 2>(a, num_sms, s, launched);
     else if (a.E <= 32)
         err = launch_cluster_any<16, 2, 4, 1, 2>(a, num_sms, s, launched);
