@@ -181,13 +181,15 @@ ORDER_CASES = [
 ]
 
 
+@pytest.mark.parametrize("via", ["route", "layer"])
 @pytest.mark.parametrize("E", [2, 8, 16, 32, 64, 200])
 @pytest.mark.parametrize("case", range(len(ORDER_CASES)))
-def test_route_canonical_order(lib, E, case):
+def test_route_canonical_order(lib, E, case, via):
     """The router's logits follow the canonical order bit for bit: expert 0's
     logit is 1 or 0 depending on the order, expert 1's is exactly 0.5, every
     other expert's is -1; the top-2 ids and weights reveal expert 0's value.
-    E spans every expert-block variant of the kernel."""
+    E spans every router variant: moe_route alone (no scratch) and the layer
+    call (whose workspace lets E > 8 run as expert slices plus a top-k pass)."""
     H, placements, want = ORDER_CASES[case]
     x = torch.zeros(1, H)
     Wg = torch.zeros(H, E)
@@ -198,7 +200,15 @@ def test_route_canonical_order(lib, E, case):
     Wg[h0, 1] = 0.5
     Wg[h0, 2:] = -1.0
     dims = lib.make_dims(1, H, 64, E, 2)
-    idx, w = lib.route(dims, x.bfloat16().cuda(), Wg.bfloat16().cuda())
+    if via == "route":
+        idx, w = lib.route(dims, x.bfloat16().cuda(), Wg.bfloat16().cuda())
+    else:
+        zeros = [torch.zeros(E, a, b, dtype=torch.bfloat16, device="cuda") for a, b in ((H, 64), (H, 64), (64, H))]
+        routing = lib.routing_buffers(dims, "cuda")
+        ws = lib.workspace(dims)
+        lib.layer_forward(dims, x.bfloat16().cuda(), Wg.bfloat16().cuda(), *zeros, ws, routing=routing)
+        assert lib.check(ws) == lib.MOE_OK
+        idx, w = routing.topk_idx, routing.topk_w
     torch.cuda.synchronize()
     idx, w = idx.cpu().tolist()[0], w.cpu().double().numpy()[0]
     assert idx == ([0, 1] if want == 1.0 else [1, 0])
@@ -227,14 +237,18 @@ ROUTE_ONLY_CASES = [
     (5003, 320, 8, 3),
     (4999, 256, 6, 2),
     (9000, 128, 3, 1),
+    (3001, 576, 64, 6),
+    (2047, 256, 16, 4),
 ]
 
 
+@pytest.mark.parametrize("via", ["route", "layer"])
 @pytest.mark.parametrize("biased", [False, True])
 @pytest.mark.parametrize("renormalize", [True, False])
 @pytest.mark.parametrize("case", ROUTE_ONLY_CASES)
-def test_route_only(lib, oracle, case, biased, renormalize):
-    """moe_route alone against the oracle: ids bit-exact, weights to 1e-5."""
+def test_route_only(lib, oracle, case, biased, renormalize, via):
+    """The routing against the oracle, from moe_route alone and from the layer
+    call: ids bit-exact, weights to 1e-5."""
     T, H, E, k = case
     inp = make_inputs(T, H, 64, E, seed=5)
     b = {n: bf16_bits(v) for n, v in inp.items()}
@@ -246,6 +260,15 @@ def test_route_only(lib, oracle, case, biased, renormalize):
                        bias=None if bias is None else torch.from_numpy(bias).cuda(),
                        renormalize=renormalize)
     torch.cuda.synchronize()
+    if via == "layer":
+        # the same routing from the layer call (the sliced router for E > 8)
+        routing = lib.routing_buffers(dims, "cuda")
+        ws = lib.workspace(dims)
+        lib.layer_forward(dims, inp["x"].cuda(), inp["Wg"].cuda(), inp["W1"].cuda(), inp["W3"].cuda(),
+                          inp["W2"].cuda(), ws, bias=None if bias is None else torch.from_numpy(bias).cuda(),
+                          routing=routing, renormalize=renormalize)
+        assert lib.check(ws) == lib.MOE_OK
+        idx, w = routing.topk_idx, routing.topk_w
     logits, ridx, rw = oracle.route(b["x"], b["Wg"], k, bias)
     if not renormalize:
         rw = oracle.gate_weights_full(logits, ridx)

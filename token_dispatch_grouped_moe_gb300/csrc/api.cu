@@ -100,7 +100,7 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, arrive, sgate, total;
+    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, arrive, sgate, logits, total;
 };
 
 Layout layout_of(const moe_dims& d)
@@ -124,6 +124,7 @@ Layout layout_of(const moe_dims& d)
     L.slot = o; o += al256(((size_t)d.k + (d.F_shared > 0 ? 1 : 0)) * T * (size_t)d.H * 4);
     L.arrive = o; o += al256(T * (size_t)((d.H + 255) / 256) * 4);
     L.sgate = o; o += al256(T * 4);
+    L.logits = o; o += al256(E > 8 ? T * E * 4 : 0);   // the sliced router's logits
     L.total = o;
     return L;
 }
@@ -482,6 +483,7 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     RouteArgs ra{x, Wg, bias, idx, tw, d.T, d.H, d.E, d.k};
     ra.renorm = gating ? (gating->renormalize != 0) : 1;
     ra.err = err;
+    ra.logits = reinterpret_cast<float*>(w + L.logits);
     MOE_TRY(launch_route(ra, sms, s));
 
     record(events ? events->before_permute : nullptr, s);

@@ -22,6 +22,7 @@ struct RouteArgs {
     int32_t H, E, k;
     int32_t renorm = 1;    // 1: softmax over the k selected; 0: over all E
     uint32_t* err = nullptr;   // device error word (a bounded wait that ran out), or null
+    float* logits = nullptr;   // [T,E] fp32 scratch for E > 8 (the sliced router), or null
 };
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s);
 

@@ -776,7 +776,7 @@ struct SShape {
 template <class S>
 __global__ void __launch_bounds__(S::THREADS, 1)
     route_stream_kernel(const __grid_constant__ CUtensorMap gmap, const __grid_constant__ CUtensorMap xmap,
-                        RouteArgs a, int gate_tma)
+                        RouteArgs a, int gate_tma, int n_sl)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     constexpr int NT = S::NT, D = S::D, NW = S::NW;
@@ -799,7 +799,20 @@ __global__ void __launch_bounds__(S::THREADS, 1)
         for (int b = 0; b < NW * D; ++b) mbar_init(smem_u32(gbar + n_steps + b), 1);
         fence_barrier_init();
     }
-    if (!gate_tma) {
+    // expert slice: with n_sl > 1 a CTA computes the logits of experts
+    // 8*slice .. 8*slice+7 only; CTAs b = n_sl*r .. n_sl*r+n_sl-1 (one stream
+    // r) take the same tokens at the same time, so x is read from HBM about once
+    const int slice = blockIdx.x % n_sl;
+    if (n_sl > 1) {
+        for (int h = threadIdx.x; h < n_steps * 256; h += S::THREADS) {
+            const int c = h >> 3, i = h & 7;
+            const bool in = h < H;
+            cp_async_16(smem_u32(gate + (size_t)c * 128 + ((i ^ (c & 7)) << 4)),
+                        in ? a.Wg + (int64_t)h * E + 8 * slice : a.Wg, in ? 16u : 0u);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+    } else if (!gate_tma) {
         for (int h = threadIdx.x; h < n_steps * 256; h += S::THREADS) {
             uint32_t w[4] = {0, 0, 0, 0};
             if (h < H)
@@ -818,10 +831,11 @@ __global__ void __launch_bounds__(S::THREADS, 1)
         }
     }
 
-    // token groups: warp w of CTA b takes g = b + grid * (w + NW * j), j = 0, 1, ..
+    // token groups: warp w of stream r takes g = r + n_streams * (w + NW * j), j = 0, 1, ..
     const int64_t G = (a.T + NT - 1) / NT;
-    const int64_t g_first = blockIdx.x + (int64_t)gridDim.x * warp;
-    const int64_t g_stride = (int64_t)gridDim.x * NW;
+    const int n_streams = gridDim.x / n_sl;
+    const int64_t g_first = blockIdx.x / n_sl + (int64_t)n_streams * warp;
+    const int64_t g_stride = (int64_t)n_streams * NW;
 
     // prefetch cursor, D-1 steps ahead; lane 0 issues the copies
     int64_t pf_g = g_first;
@@ -903,6 +917,20 @@ __global__ void __launch_bounds__(S::THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) v[tt * 8 + e] = acc[tt][e];
         transpose_reduce<NT * 8, 16>(v, lane);
+        if (n_sl > 1) {
+            // this slice's logits (bias added) for the top-k pass
+            const int64_t t = g * NT + my_tt;
+            if ((lane & ((1 << LOG_DUP) - 1)) == 0 && t < a.T) {
+#pragma unroll
+                for (int u = 0; u < NV; ++u) {
+                    const int e = 8 * slice + e0 + u;
+                    float l = v[u];
+                    if (a.bias) l = l + a.bias[e];
+                    a.logits[t * E + e] = l;
+                }
+            }
+            continue;
+        }
         float l[NV];
 #pragma unroll
         for (int u = 0; u < NV; ++u) {
@@ -971,10 +999,80 @@ __global__ void __launch_bounds__(S::THREADS, 1)
         for (int m = 0; m < n_steps; ++m) mbar_wait_drain(smem_u32(gbar + m), 0);
 }
 
-// Returns false (nothing launched) when a tensor map cannot be made.
+// Top-k and gate weights from the [T, E] logits the sliced router wrote: one
+// warp per token, lane l holds experts l, l+32, ..; k rounds of a warp argmax
+// (larger logit, ties to the lower id).
+__global__ void route_topk_kernel(RouteArgs a)
+{
+    const int lane = threadIdx.x & 31;
+    const int E = a.E, k = a.k;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.T; t += warps) {
+        const float* l = a.logits + t * E;
+        float lv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) lv[u] = (lane + 32 * u < E) ? l[lane + 32 * u] : 0.0f;
+        uint32_t taken = 0;
+        int sel_e[8];
+        float sel_l[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j >= k) break;
+            float bv = 0.0f;
+            int be = -1;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const bool ok = (lane + 32 * u < E) && !((taken >> u) & 1u);
+                if (ok && (be < 0 || lv[u] > bv)) { bv = lv[u]; be = lane + 32 * u; }
+            }
+#pragma unroll
+            for (int st = 16; st >= 1; st >>= 1) {
+                const float ov = __shfl_xor_sync(kFull, bv, st);
+                const int oe = __shfl_xor_sync(kFull, be, st);
+                const bool better = (oe >= 0) && (be < 0 || ov > bv || (ov == bv && oe < be));
+                if (better) { bv = ov; be = oe; }
+            }
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            sel_e[j] = be;
+            sel_l[j] = bv;
+        }
+        const float mx = sel_l[0];
+        // without renormalisation the denominator runs over all E experts
+        float den_all = 0.0f;
+        if (!a.renorm) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (lane + 32 * u < E) den_all += expf(lv[u] - mx);
+#pragma unroll
+            for (int st = 16; st >= 1; st >>= 1) den_all += __shfl_xor_sync(kFull, den_all, st);
+        }
+        if (lane == 0) {
+            float ex[8];
+            float den = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= k) break;
+                ex[j] = expf(sel_l[j] - mx);
+                den = den + ex[j];
+            }
+            if (!a.renorm) den = den_all;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                if (j >= k) break;
+                a.topk_idx[t * k + j] = sel_e[j];
+                a.topk_w[t * k + j] = ex[j] / den;
+            }
+        }
+    }
+}
+
+// Returns false (nothing launched) when a tensor map cannot be made. With
+// E > 8 (a multiple of 8, a.logits set) the experts are split in slices of 8
+// over the CTAs of a stream and a second kernel takes the top-k.
 template <class S>
 bool launch_stream(const RouteArgs& a, int num_sms, cudaStream_t s, cudaError_t& err)
 {
+    const int n_sl = a.E > 8 ? a.E / 8 : 1;
     CUtensorMap gmap, xmap;
     std::memset(&gmap, 0, sizeof(gmap));
     // x as a bf16 [T, H] matrix, box {256, NT}: one step of NT token rows
@@ -985,12 +1083,18 @@ bool launch_stream(const RouteArgs& a, int num_sms, cudaStream_t s, cudaError_t&
     auto kern = route_stream_kernel<S>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return true;
-    // one CTA per SM while there are groups for each: the groups are dealt
-    // round-robin over the CTAs first, so every SM gets within one of the same
-    // number of groups
+    // one CTA per SM; the token groups are dealt round-robin over the streams
+    // (n_sl CTAs each), so every SM gets within one of the same number
     const int64_t G = (a.T + S::NT - 1) / S::NT;
-    const int grid = (int)(G < num_sms ? G : num_sms);
-    kern<<<grid, S::THREADS, smem, s>>>(gmap, xmap, a, gate_tma ? 1 : 0);
+    int64_t n_streams = num_sms / n_sl;
+    if (n_streams > G) n_streams = G;
+    if (n_streams < 1) n_streams = 1;
+    kern<<<(unsigned)(n_streams * n_sl), S::THREADS, smem, s>>>(gmap, xmap, a, gate_tma ? 1 : 0, n_sl);
+    err = cudaGetLastError();
+    if (err != cudaSuccess || n_sl == 1) return true;
+    const int64_t blocks = (a.T + 7) / 8;
+    const int64_t cap = (int64_t)num_sms * 8;
+    route_topk_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(a);
     err = cudaGetLastError();
     return true;
 }
@@ -1007,6 +1111,10 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s)
     if (a.E <= 8) {
         if (SShape<8, 4, 8>::smem_bytes(a.H) <= kStreamBudget && launch_stream<SShape<8, 4, 8>>(a, num_sms, s, err))
             return err;
+    } else if (a.logits && a.E % 8 == 0 && SShape<8, 4, 8>::smem_bytes(a.H) <= kStreamBudget &&
+               launch_stream<SShape<8, 4, 8>>(a, num_sms, s, err)) {
+        // E > 8 with room for the logits: expert slices plus a top-k pass
+        return err;
     } else if (a.E <= 16)
         err = launch_cluster_any<16, 1, 2, 1, 2>(a, num_sms, s, launched);
     else if (a.E <= 32)
