@@ -999,69 +999,79 @@ __global__ void __launch_bounds__(S::THREADS, 1)
         for (int m = 0; m < n_steps; ++m) mbar_wait_drain(smem_u32(gbar + m), 0);
 }
 
-// Top-k and gate weights from the [T, E] logits the sliced router wrote: one
-// warp per token, lane l holds experts l, l+32, ..; k rounds of a warp argmax
-// (larger logit, ties to the lower id).
+// Top-k and gate weights from the [T, E] logits the sliced router wrote. A
+// warp takes 4 tokens, 8 lanes per token; lane r of a token holds experts
+// r*E/8 .. r*E/8 + E/8 - 1 (E is a multiple of 8, at most 256). k rounds of
+// an argmax (larger logit, ties to the lower id) over the token's 8 lanes.
 __global__ void route_topk_kernel(RouteArgs a)
 {
     const int lane = threadIdx.x & 31;
+    const int r = lane & 7;
     const int E = a.E, k = a.k;
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < a.T; t += warps) {
-        const float* l = a.logits + t * E;
-        float lv[8];
+    const int per = E >> 3;   // logits per lane
+    const int64_t t = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 4 + (lane >> 3);
+    const bool live = t < a.T;
+    const int e_lo = r * per;
+    float lv[32];
+    const float* src = a.logits + t * E + e_lo;
+    if ((per & 3) == 0) {   // 16-byte aligned runs of 4
 #pragma unroll
-        for (int u = 0; u < 8; ++u) lv[u] = (lane + 32 * u < E) ? l[lane + 32 * u] : 0.0f;
-        uint32_t taken = 0;
-        int sel_e[8];
-        float sel_l[8];
+        for (int u = 0; u < 32; u += 4) {
+            float4 q = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (live && u < per) q = *reinterpret_cast<const float4*>(src + u);
+            lv[u] = q.x; lv[u + 1] = q.y; lv[u + 2] = q.z; lv[u + 3] = q.w;
+        }
+    } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) lv[u] = (live && u < per) ? src[u] : 0.0f;
+    }
+    uint32_t taken = 0;
+    int sel_e[8];
+    float sel_l[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j >= k) break;
+        float bv = 0.0f;
+        int be = -1;
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+            if (u < per && !((taken >> u) & 1u) && (be < 0 || lv[u] > bv)) { bv = lv[u]; be = e_lo + u; }
+#pragma unroll
+        for (int st = 1; st < 8; st <<= 1) {
+            const float ov = __shfl_xor_sync(kFull, bv, st);
+            const int oe = __shfl_xor_sync(kFull, be, st);
+            const bool better = (oe >= 0) && (be < 0 || ov > bv || (ov == bv && oe < be));
+            if (better) { bv = ov; be = oe; }
+        }
+        if (be >= e_lo && be < e_lo + per) taken |= 1u << (be - e_lo);
+        sel_e[j] = be;
+        sel_l[j] = bv;
+    }
+    const float mx = sel_l[0];
+    // without renormalisation the denominator runs over all E experts
+    float den_all = 0.0f;
+    if (!a.renorm) {
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+            if (u < per) den_all = den_all + expf(lv[u] - mx);
+#pragma unroll
+        for (int st = 1; st < 8; st <<= 1) den_all = den_all + __shfl_xor_sync(kFull, den_all, st);
+    }
+    if (r == 0 && live) {
+        float ex[8];
+        float den = 0.0f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             if (j >= k) break;
-            float bv = 0.0f;
-            int be = -1;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const bool ok = (lane + 32 * u < E) && !((taken >> u) & 1u);
-                if (ok && (be < 0 || lv[u] > bv)) { bv = lv[u]; be = lane + 32 * u; }
-            }
-#pragma unroll
-            for (int st = 16; st >= 1; st >>= 1) {
-                const float ov = __shfl_xor_sync(kFull, bv, st);
-                const int oe = __shfl_xor_sync(kFull, be, st);
-                const bool better = (oe >= 0) && (be < 0 || ov > bv || (ov == bv && oe < be));
-                if (better) { bv = ov; be = oe; }
-            }
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-            sel_e[j] = be;
-            sel_l[j] = bv;
+            ex[j] = expf(sel_l[j] - mx);
+            den = den + ex[j];
         }
-        const float mx = sel_l[0];
-        // without renormalisation the denominator runs over all E experts
-        float den_all = 0.0f;
-        if (!a.renorm) {
+        if (!a.renorm) den = den_all;
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (lane + 32 * u < E) den_all += expf(lv[u] - mx);
-#pragma unroll
-            for (int st = 16; st >= 1; st >>= 1) den_all += __shfl_xor_sync(kFull, den_all, st);
-        }
-        if (lane == 0) {
-            float ex[8];
-            float den = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (j >= k) break;
-                ex[j] = expf(sel_l[j] - mx);
-                den = den + ex[j];
-            }
-            if (!a.renorm) den = den_all;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if (j >= k) break;
-                a.topk_idx[t * k + j] = sel_e[j];
-                a.topk_w[t * k + j] = ex[j] / den;
-            }
+        for (int j = 0; j < 8; ++j) {
+            if (j >= k) break;
+            a.topk_idx[t * k + j] = sel_e[j];
+            a.topk_w[t * k + j] = ex[j] / den;
         }
     }
 }
@@ -1092,9 +1102,7 @@ bool launch_stream(const RouteArgs& a, int num_sms, cudaStream_t s, cudaError_t&
     kern<<<(unsigned)(n_streams * n_sl), S::THREADS, smem, s>>>(gmap, xmap, a, gate_tma ? 1 : 0, n_sl);
     err = cudaGetLastError();
     if (err != cudaSuccess || n_sl == 1) return true;
-    const int64_t blocks = (a.T + 7) / 8;
-    const int64_t cap = (int64_t)num_sms * 8;
-    route_topk_kernel<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, s>>>(a);
+    route_topk_kernel<<<(unsigned)((a.T + 31) / 32), 256, 0, s>>>(a);   // 8 warps x 4 tokens
     err = cudaGetLastError();
     return true;
 }
