@@ -35,6 +35,10 @@ sys.path.insert(0, ROOT)
 from token_dispatch_grouped_moe_gb300.configs import CONFIGS  # noqa: E402
 
 METRIC = "MoE layer fwd bf16 TFLOP/s & tokens/s on 1 GB300; % of tensor peak / HBM BW"
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM0 launch, from a
+# one-pass ncu capture of this benchmark at the configuration's full size; configurations
+# without such a capture report null
+GEMM0_TRAFFIC = {"mixtral": 2014245120 + 457582080}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -177,6 +181,8 @@ def bench_ours(args, cfg):
     if not os.path.exists(lib.LIB_PATH):
         cuda_build.build()
     lib.load()
+    lib.set_combine({"auto": lib.COMBINE_AUTO, "fused": lib.COMBINE_FUSED,
+                     "separate": lib.COMBINE_SEPARATE}[args.combine])
 
     inp, g = make_workload(cfg, device)
     dims = lib.make_dims(cfg.T, cfg.H, cfg.F, cfg.E, cfg.k, cfg.Fs)
@@ -288,8 +294,11 @@ def bench_ours(args, cfg):
     stage_roofline["route"]["frac"] = round(stage_roofline["route"]["gbs"] / peaks["hbm_gbs"], 4)
 
     value = world * flops / (ms * 1e-3) / 1e12
-    # route; histogram, scatter, x_perm gather; GEMM0, GEMM1 (+ combine); shared GEMMs
-    launches_per_step = 1 + 3 + 2 + (2 if cfg.Fs else 0)
+    # route (+ the top-k pass of the sliced router, E > 8); histogram, scatter,
+    # x_perm gather; GEMM0, GEMM1; shared GEMMs; a separate combine unless fused
+    fused = args.combine == "fused" or (args.combine == "auto" and (cfg.Fs or cfg.F) >= 4096)
+    route_launches = 2 if (cfg.E > 8 and cfg.E % 8 == 0) else 1
+    launches_per_step = route_launches + 3 + 2 + (2 if cfg.Fs else 0) + (0 if fused else 1)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -311,7 +320,8 @@ def bench_ours(args, cfg):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "kernel": "grouped GEMM0 + SwiGLU (tcgen05)",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": GEMM0_TRAFFIC.get(cfg.name),
+                     "traffic_unit": "bytes per launch",
                      "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"},
         "stage_ms": stage_summary,
         "stage_roofline": stage_roofline,
@@ -389,6 +399,8 @@ def main():
     ap.add_argument("--config", default="mixtral", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--combine", default="auto", choices=["auto", "fused", "separate"],
+                    help="where the layer sums the expert rows (GEMM1 epilogue or a separate kernel)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--ref-tokens", type=int, default=64, help="oracle tokens per reference step")
     args = ap.parse_args()

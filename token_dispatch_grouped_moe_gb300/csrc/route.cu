@@ -1003,6 +1003,9 @@ __global__ void __launch_bounds__(S::THREADS, 1)
 // warp takes 4 tokens, 8 lanes per token; lane r of a token holds experts
 // r*E/8 .. r*E/8 + E/8 - 1 (E is a multiple of 8, at most 256). k rounds of
 // an argmax (larger logit, ties to the lower id) over the token's 8 lanes.
+// PMAX bounds E/8 at compile time, so the per-lane loops are no longer than
+// the logits a lane holds.
+template <int PMAX>
 __global__ void route_topk_kernel(RouteArgs a)
 {
     const int lane = threadIdx.x & 31;
@@ -1012,18 +1015,18 @@ __global__ void route_topk_kernel(RouteArgs a)
     const int64_t t = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 4 + (lane >> 3);
     const bool live = t < a.T;
     const int e_lo = r * per;
-    float lv[32];
+    float lv[PMAX];
     const float* src = a.logits + t * E + e_lo;
     if ((per & 3) == 0) {   // 16-byte aligned runs of 4
 #pragma unroll
-        for (int u = 0; u < 32; u += 4) {
+        for (int u = 0; u < PMAX; u += 4) {
             float4 q = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             if (live && u < per) q = *reinterpret_cast<const float4*>(src + u);
             lv[u] = q.x; lv[u + 1] = q.y; lv[u + 2] = q.z; lv[u + 3] = q.w;
         }
     } else {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) lv[u] = (live && u < per) ? src[u] : 0.0f;
+        for (int u = 0; u < PMAX; ++u) lv[u] = (live && u < per) ? src[u] : 0.0f;
     }
     uint32_t taken = 0;
     int sel_e[8];
@@ -1034,7 +1037,7 @@ __global__ void route_topk_kernel(RouteArgs a)
         float bv = 0.0f;
         int be = -1;
 #pragma unroll
-        for (int u = 0; u < 32; ++u)
+        for (int u = 0; u < PMAX; ++u)
             if (u < per && !((taken >> u) & 1u) && (be < 0 || lv[u] > bv)) { bv = lv[u]; be = e_lo + u; }
 #pragma unroll
         for (int st = 1; st < 8; st <<= 1) {
@@ -1052,7 +1055,7 @@ __global__ void route_topk_kernel(RouteArgs a)
     float den_all = 0.0f;
     if (!a.renorm) {
 #pragma unroll
-        for (int u = 0; u < 32; ++u)
+        for (int u = 0; u < PMAX; ++u)
             if (u < per) den_all = den_all + expf(lv[u] - mx);
 #pragma unroll
         for (int st = 1; st < 8; st <<= 1) den_all = den_all + __shfl_xor_sync(kFull, den_all, st);
@@ -1102,7 +1105,15 @@ bool launch_stream(const RouteArgs& a, int num_sms, cudaStream_t s, cudaError_t&
     kern<<<(unsigned)(n_streams * n_sl), S::THREADS, smem, s>>>(gmap, xmap, a, gate_tma ? 1 : 0, n_sl);
     err = cudaGetLastError();
     if (err != cudaSuccess || n_sl == 1) return true;
-    route_topk_kernel<<<(unsigned)((a.T + 31) / 32), 256, 0, s>>>(a);   // 8 warps x 4 tokens
+    const unsigned blocks = (unsigned)((a.T + 31) / 32);   // 8 warps x 4 tokens
+    if (n_sl <= 4)
+        route_topk_kernel<4><<<blocks, 256, 0, s>>>(a);
+    else if (n_sl <= 8)
+        route_topk_kernel<8><<<blocks, 256, 0, s>>>(a);
+    else if (n_sl <= 16)
+        route_topk_kernel<16><<<blocks, 256, 0, s>>>(a);
+    else
+        route_topk_kernel<32><<<blocks, 256, 0, s>>>(a);
     err = cudaGetLastError();
     return true;
 }
