@@ -134,7 +134,19 @@ enum {
     MOE_OPT_COMBINE = 1,
     MOE_COMBINE_AUTO = 0,
     MOE_COMBINE_FUSED = 1,
-    MOE_COMBINE_SEPARATE = 2
+    MOE_COMBINE_SEPARATE = 2,
+    /* Whether moe_layer_forward runs the routed experts' two GEMMs as one
+     * persistent launch (GEMM1 tiles start as soon as the GEMM0 tiles of their
+     * expert and 128-row block have written h; no launch boundary, no GEMM0
+     * tail) or as two launches. Only with MOE_GEMM0_A_PERMUTED.
+     *   MOE_GEMM_FUSION_AUTO (default) the table in the library's layer call
+     *                        (by shape; see moe_layer_forward);
+     *   MOE_GEMM_FUSION_ON / MOE_GEMM_FUSION_OFF force it.
+     * Same arithmetic either way: bit-identical. */
+    MOE_OPT_GEMM_FUSION = 2,
+    MOE_GEMM_FUSION_AUTO = 0,
+    MOE_GEMM_FUSION_ON = 1,
+    MOE_GEMM_FUSION_OFF = 2
 };
 
 /* Sets a library-wide option for later calls (all devices and threads).

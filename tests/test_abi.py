@@ -94,13 +94,18 @@ def test_options(L):
     assert lib.get_gemm0_a() == lib.GEMM0_A_TMA_GATHER
     lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
     assert L.moe_set_option(0, 7) == 1
-    assert L.moe_set_option(3, 0) == 1
-    assert L.moe_get_option(3) == -1
+    assert L.moe_set_option(4, 0) == 1
+    assert L.moe_get_option(4) == -1
     assert lib.get_combine() == lib.COMBINE_AUTO
     for mode in (lib.COMBINE_FUSED, lib.COMBINE_SEPARATE, lib.COMBINE_AUTO):
         lib.set_combine(mode)
         assert lib.get_combine() == mode
     assert L.moe_set_option(1, 3) == 1
+    assert lib.get_gemm_fusion() == lib.GEMM_FUSION_AUTO
+    for mode in (lib.GEMM_FUSION_ON, lib.GEMM_FUSION_OFF, lib.GEMM_FUSION_AUTO):
+        lib.set_gemm_fusion(mode)
+        assert lib.get_gemm_fusion() == mode
+    assert L.moe_set_option(2, 3) == 1
 
 
 def test_zero_tokens_is_noop_on_host(L):

@@ -361,6 +361,46 @@ def test_combine_forms_bit_identical(lib, shape):
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
 
 
+@pytest.mark.parametrize("shape", [(300, 256, 192, 8, 2, 0), (257, 192, 128, 64, 6, 0),
+                                   (200, 256, 128, 16, 4, 384), (64, 128, 64, 256, 8, 0),
+                                   (1500, 512, 1408, 8, 2, 0), (3, 64, 64, 3, 2, 0)])
+def test_gemm_fusion_bit_identical(lib, shape):
+    """Both routed GEMMs in one persistent launch (GEMM1 tiles wait for their
+    rows of h) give the same bits as two launches, with either combine form."""
+    T, H, F, E, k, Fs = shape
+    inp = make_inputs(T, H, F, E, Fs=Fs, seed=11)
+    g = {n: v.cuda() for n, v in inp.items()}
+    dims = lib.make_dims(T, H, F, E, k, Fs)
+    ws = lib.workspace(dims)
+    outs = []
+    try:
+        for combine in (lib.COMBINE_SEPARATE, lib.COMBINE_FUSED):
+            lib.set_combine(combine)
+            for fusion in (lib.GEMM_FUSION_OFF, lib.GEMM_FUSION_ON, lib.GEMM_FUSION_ON):
+                lib.set_gemm_fusion(fusion)
+                outs.append(lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws,
+                                              W1s=g.get("W1s"), W3s=g.get("W3s"),
+                                              W2s=g.get("W2s")).clone())
+    finally:
+        lib.set_combine(lib.COMBINE_AUTO)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "f_tail", "h_tail_e64", "shared", "one_token", "e256"])
+def test_small_case_fused_gemms(lib, oracle, name):
+    """Edge cases with both routed GEMMs in one launch, against the oracle."""
+    T, H, F, E, k, Fs = SMALL_CASES[name]
+    lib.set_gemm_fusion(lib.GEMM_FUSION_ON)
+    try:
+        run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=3, tol="elementwise")
+    finally:
+        lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
+
+
 @pytest.mark.parametrize("name", ["tiny", "f_tail", "h_tail_e64", "shared", "e256"])
 def test_small_case_fused_combine(lib, oracle, name):
     """Edge cases with the combine fused into GEMM1 forced on."""

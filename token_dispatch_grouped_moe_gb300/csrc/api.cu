@@ -24,6 +24,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<int> g_num_sms[kMaxDevices];
 std::atomic<int> g_gemm0_a{MOE_GEMM0_A_PERMUTED};
 std::atomic<int> g_combine{MOE_COMBINE_AUTO};
+std::atomic<int> g_gemm_fusion{MOE_GEMM_FUSION_AUTO};
 
 int num_sms_current()
 {
@@ -95,12 +96,23 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
     return encode_map_2d(m, base, inner, outer, 64, box_outer, true);
 }
 
+// The shapes for which one launch of both routed GEMMs measured faster than
+// two (MOE_GEMM_FUSION_AUTO): fewer than 512 routed rows per expert on
+// average, where the GEMMs are short (a few waves of tiles, weight-bandwidth
+// bound) and the GEMM0 tail and launch boundary weigh (DeepSeek-shaped T=1024:
+// 0.273 -> 0.259 ms per layer, T=4096: 0.484 -> 0.468 ms). From 512 rows per
+// expert up (Qwen2, DeepSeek T=32768, Mixtral) the two forms measured the same.
+bool auto_fuse_gemms(const moe_dims& d)
+{
+    return d.T * (int64_t)d.k < (int64_t)512 * d.E;
+}
+
 // ------------------------------------------------------------ workspace --
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, arrive, sgate, logits, total;
+    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, arrive, sgate, logits, ready, total;
 };
 
 Layout layout_of(const moe_dims& d)
@@ -125,6 +137,7 @@ Layout layout_of(const moe_dims& d)
     L.arrive = o; o += al256(T * (size_t)((d.H + 255) / 256) * 4);
     L.sgate = o; o += al256(T * 4);
     L.logits = o; o += al256(E > 8 ? T * E * 4 : 0);   // the sliced router's logits
+    L.ready = o; o += al256(((R + kTileM - 1) / kTileM + E + 1) * 4);   // fused GEMMs: per M tile
     L.total = o;
     return L;
 }
@@ -197,7 +210,7 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
                             const uint16_t* W3, const uint16_t* W2, const float* topk_w, float* slot,
                             uint16_t* h, uint32_t* err, int sms, cudaStream_t s, moe_event_t ev_mid,
                             const FusedCombine& fc = FusedCombine{false, 0, 0, nullptr, nullptr},
-                            bool cp_gather = false)
+                            bool cp_gather = false, int32_t* ready = nullptr)
 {
     if (M == 0) {
         if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
@@ -227,6 +240,26 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
     a.K = d.H;
     a.h_out = reinterpret_cast<__nv_bfloat16*>(h);
     a.x = x;
+    if (ready && dense) {
+        // both GEMMs in one launch: GEMM1 tiles wait for their rows of h
+        GemmArgs b = a;
+        b.N = d.H;
+        b.K = F;
+        b.h_out = nullptr;
+        b.topk_w = topk_w;
+        b.slot = slot;
+        b.slot_j0 = fc.on ? fc.slot_j0 : 0;
+        b.n_slots = fc.n_slots;
+        b.arrive = fc.arrive;
+        b.out = fc.out;
+        b.ready = ready;
+        b.ready_target = 4 * ((F + 127) / 128);   // 4 epilogue warps x GEMM0 N tiles
+        MOE_TRY(cudaMemsetAsync(ready, 0, (size_t)((M + kTileM - 1) / kTileM + G + 1) * 4, s));
+        MOE_TRY(launch_grouped_gemm_fused(fc.on ? kFusedCombine : kFusedScatter, mx, m1, m3, mh, m2, a, b,
+                                          sms, s));
+        if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
+        return MOE_OK;
+    }
     MOE_TRY(launch_grouped_gemm(dense ? kGemm0Dense : cp_gather ? kGemm0CpGather : kGemm0Gather, mx, m1,
                                 m3, a, sms, s));
     if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
@@ -287,6 +320,12 @@ moe_status moe_set_option(int option, int value)
         g_combine.store(value);
         return MOE_OK;
     }
+    if (option == MOE_OPT_GEMM_FUSION) {
+        if (value != MOE_GEMM_FUSION_AUTO && value != MOE_GEMM_FUSION_ON && value != MOE_GEMM_FUSION_OFF)
+            return MOE_ERR_INVALID_ARG;
+        g_gemm_fusion.store(value);
+        return MOE_OK;
+    }
     return MOE_ERR_INVALID_ARG;
 }
 
@@ -294,6 +333,7 @@ int moe_get_option(int option)
 {
     if (option == MOE_OPT_GEMM0_A) return g_gemm0_a.load();
     if (option == MOE_OPT_COMBINE) return g_combine.load();
+    if (option == MOE_OPT_GEMM_FUSION) return g_gemm_fusion.load();
     return -1;
 }
 
@@ -498,12 +538,18 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     if (permuted)
         MOE_TRY(launch_gather_rows(x, src, offsets + d.E, xp, R, d.T, d.H, d.k, err, sms, s));
 
+    // both routed GEMMs in one launch (dense A only)
+    const int fusion_opt = g_gemm_fusion.load();
+    const bool fuse_gemms = permuted && (fusion_opt == MOE_GEMM_FUSION_ON ||
+                                         (fusion_opt == MOE_GEMM_FUSION_AUTO && auto_fuse_gemms(d)));
+
     record(events ? events->before_gemm0 : nullptr, s);
     MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)R, d.F, d.E, d.k, x, permuted ? xp : nullptr, src,
                                     tile, offsets, W1, W3, W2, tw, slot,
                                     reinterpret_cast<uint16_t*>(w + L.h), err, sms, s,
                                     events ? events->before_gemm1 : nullptr,
-                                    FusedCombine{fused, 0, n_slots, arrive, out}, cp_gather));
+                                    FusedCombine{fused, 0, n_slots, arrive, out}, cp_gather,
+                                    fuse_gemms ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr));
 
     record(events ? events->before_shared : nullptr, s);
     if (d.F_shared > 0) {

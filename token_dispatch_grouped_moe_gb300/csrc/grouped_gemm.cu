@@ -113,10 +113,38 @@ __device__ __forceinline__ Work decode_work(int w, int n_tiles, const int* ts, c
     return r;
 }
 
+// Waits until *ctr >= target (acquire, GPU scope). Returns false (after
+// recording a timeout and raising *abort) if that takes longer than
+// kWaitLimitNs of %globaltimer time or another role has aborted.
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int32_t target, volatile int* abort,
+                                           uint32_t* err)
+{
+    auto load = [&]() {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        return v;
+    };
+    if (load() >= target) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(128);
+        if (load() >= target) return true;
+        if ((i & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                report_error(err, MOE_DEV_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const GemmArgs args)
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmA1,
+                    const __grid_constant__ CUtensorMap tmB2, const GemmArgs args, const GemmArgs args1)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -124,7 +152,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     unsigned char* tiles = smem_raw + (tiles_addr - raw_addr);
     SmemTail* st = reinterpret_cast<SmemTail*>(tiles + (size_t)STAGES * STAGE_BYTES);
 
+    // FUSED: work items [0, total0) are GEMM0 (dense A) tiles, the rest GEMM1
+    // tiles (args1, maps tmA1 / tmB2); a GEMM1 tile waits until every GEMM0
+    // tile of its (expert, M tile) has published its rows of h
+    constexpr bool FUSED = (MODE == kFusedScatter || MODE == kFusedCombine);
     constexpr bool IS_GEMM0 = (MODE == kGemm0Gather || MODE == kGemm0Dense || MODE == kGemm0CpGather);
+    constexpr bool HAS_GEMM0 = IS_GEMM0 || FUSED;
+    constexpr bool COMBINE = (MODE == kGemm1Combine || MODE == kFusedCombine);
     constexpr bool CP_GATHER = (MODE == kGemm0CpGather);
     constexpr bool GATHER = (MODE == kGemm0Gather);
     const int warp = threadIdx.x >> 5;
@@ -163,7 +197,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB0);
-        if (IS_GEMM0) tma_prefetch_desc(&tmB1);
+        if (HAS_GEMM0) tma_prefetch_desc(&tmB1);
+        if (FUSED) {
+            tma_prefetch_desc(&tmA1);
+            tma_prefetch_desc(&tmB2);
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&st->tmem_base), TMEM_COLS);
@@ -174,10 +212,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tc_fence_after();
 
     const uint32_t tmem_base = st->tmem_base;
-    const int n_out = IS_GEMM0 ? BN / 2 : BN;   // output columns per tile
-    const int n_tiles = (args.N + n_out - 1) / n_out;
-    const int total = st->tile_start[G] * n_tiles;
-    const int k_blocks = args.K / BK;
+    // pass 0 (this mode's GEMM, or GEMM0 when fused) and pass 1 (GEMM1 when fused)
+    const int n_out0 = HAS_GEMM0 ? BN / 2 : BN;   // output columns per tile
+    const int n_tiles0 = (args.N + n_out0 - 1) / n_out0;
+    const int total0 = st->tile_start[G] * n_tiles0;
+    const int n_tiles1 = FUSED ? (args1.N + BN - 1) / BN : 0;
+    const int total = total0 + st->tile_start[G] * n_tiles1;
+    const int k_blocks0 = args.K / BK;
+    const int k_blocks1 = FUSED ? args1.K / BK : 0;
     volatile int* abort = &st->abort;
 
     if (warp == 0) {
@@ -187,7 +229,23 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int issued = 0;
         bool ok = true;
         for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-            const Work wk = decode_work(w, n_tiles, st->tile_start, st->offsets, G);
+            const bool p1 = FUSED && w >= total0;
+            const int n_tiles = p1 ? n_tiles1 : n_tiles0;
+            const int k_blocks = p1 ? k_blocks1 : k_blocks0;
+            const Work wk = decode_work(p1 ? w - total0 : w, n_tiles, st->tile_start, st->offsets, G);
+            if (p1) {
+                // the rows of h this tile reads: every GEMM0 tile of (expert, M tile)
+                // must have stored and published them
+                const int mt = st->tile_start[wk.g] + (wk.row0 - st->offsets[wk.g]) / BM;
+                bool ready = true;
+                if (lane == 0) ready = wait_count(args1.ready + mt, args1.ready_target, abort, args.err);
+                if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
+            }
             int tok[4] = {0, 0, 0, 0};
             if (GATHER) {
 #pragma unroll
@@ -202,7 +260,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     tok[r] = t;
                 }
             }
-            const int b_row = wk.g * args.K;
+            const int b_row = wk.g * (p1 ? args1.K : args.K);
             for (int kb = 0; kb < k_blocks; ++kb) {
                 // every lane waits; the outcome is made warp-uniform
                 if (!__all_sync(0xffffffffu,
@@ -218,8 +276,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (GATHER)
                     tma_gather4(a_dst + lane * 512, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], full);
                 else if (!CP_GATHER && lane == 0)
-                    tma_load_2d(a_dst, &tmA, kb * BK, wk.row0, full);
-                if (IS_GEMM0) {
+                    tma_load_2d(a_dst, p1 ? &tmA1 : &tmA, kb * BK, wk.row0, full);
+                if (HAS_GEMM0 && !p1) {
                     if (lane == 0) {
                         const int n0 = wk.n_tile * (BN / 2);
                         tma_load_2d(b_dst + 0 * B_CHUNK_BYTES, &tmB0, n0, b_row + kb * BK, full);
@@ -232,8 +290,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const int n0 = wk.n_tile * BN;
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
-                            tma_load_2d(b_dst + j * B_CHUNK_BYTES, &tmB0, n0 + 64 * j, b_row + kb * BK,
-                                        full);
+                            tma_load_2d(b_dst + j * B_CHUNK_BYTES, p1 ? &tmB2 : &tmB0, n0 + 64 * j,
+                                        b_row + kb * BK, full);
                     }
                 }
                 ++issued;
@@ -259,6 +317,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             bool ok = true;
             bool any = false;
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+                const int k_blocks = (FUSED && w >= total0) ? k_blocks1 : k_blocks0;
                 if (!mbar_wait(smem_u32(&st->tempty[acc]), acc_phase ^ 1u, abort, args.err)) {
                     ok = false;
                     break;
@@ -312,6 +371,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (++done_stage == STAGES) done_stage = 0;
                 --pending;
             };
+            const int n_tiles = n_tiles0;
+            const int k_blocks = k_blocks0;
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
                 const Work wk = decode_work(w, n_tiles, st->tile_start, st->offsets, G);
                 __syncwarp();   // the previous tile's rows are no longer read
@@ -362,14 +423,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int w = blockIdx.x; w < total; w += gridDim.x) {
-            const Work wk = decode_work(w, n_tiles, st->tile_start, st->offsets, G);
+            const bool p1 = FUSED && w >= total0;
+            const int n_tiles = p1 ? n_tiles1 : n_tiles0;
+            const Work wk = decode_work(p1 ? w - total0 : w, n_tiles, st->tile_start, st->offsets, G);
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&st->tfull[acc]), acc_phase, abort, args.err)))
                 break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + ((uint32_t)(ew * 32) << 16) + acc * BN;
             const bool valid = r < wk.rows;
             const int p = wk.row0 + r;
-            if (IS_GEMM0) {
+            if (HAS_GEMM0 && !p1) {
                 const int n0 = wk.n_tile * (BN / 2);
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
@@ -399,8 +462,21 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                          packed[8 * i + 6], packed[8 * i + 7]);
                     }
                 }
+                if constexpr (FUSED) {
+                    // publish this warp's 32 rows of the tile to the GEMM1 tiles
+                    // that read them with TMA (generic stores -> async-proxy reads)
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    __threadfence();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const int mt = st->tile_start[wk.g] + (wk.row0 - st->offsets[wk.g]) / BM;
+                        atomicAdd(args1.ready + mt, 1);
+                    }
+                }
             } else {
                 const int n0 = wk.n_tile * BN;
+                const int N1 = FUSED ? args1.N : args.N;
+                const float* topk_w = FUSED ? args1.topk_w : args.topk_w;
                 int64_t t = 0;
                 int j = 0;
                 float wt = 1.0f;
@@ -412,17 +488,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (f < 0 || t >= args.T) {
                         report_error(args.err, MOE_DEV_ERR_BOUNDS);
                         ok_row = false;
-                    } else if (args.topk_w) {
-                        wt = args.topk_w[f];
+                    } else if (topk_w) {
+                        wt = topk_w[f];
                     }
                 }
-                float* dst_row = args.slot + ((int64_t)(args.slot_j0 + j) * args.T + t) * args.N + n0;
+                float* dst_row = (FUSED ? args1.slot : args.slot) +
+                                 ((int64_t)((FUSED ? args1.slot_j0 : args.slot_j0) + j) * args.T + t) * N1 + n0;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(t_row + c, v);
                     tc_wait_ld();
-                    if (ok_row && n0 + c < args.N) {
+                    if (ok_row && n0 + c < N1) {
                         // 128 bytes of this row: four whole-sector stores
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
@@ -439,9 +516,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&st->tempty[acc]));   // TMEM free for the MMA
-            if constexpr (MODE == kGemm1Combine) {
+            if (COMBINE && (!FUSED || p1)) {
                 // publish this row's slot segment, then take a ticket for its
                 // (token, N tile); the holder of the last ticket finishes it
+                const int N1 = FUSED ? args1.N : args.N;
+                const int n_slots = FUSED ? args1.n_slots : args.n_slots;
+                float* slot = FUSED ? args1.slot : args.slot;
+                uint16_t* out = FUSED ? args1.out : args.out;
+                int32_t* arrive = FUSED ? args1.arrive : args.arrive;
                 int64_t t = -1;
                 bool last = false;
                 if (valid) {
@@ -449,7 +531,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (f >= 0 && f / args.k < args.T) {
                         t = f / args.k;
                         __threadfence();
-                        last = atomicAdd(args.arrive + t * n_tiles + wk.n_tile, 1) == args.n_slots - 1;
+                        last = atomicAdd(arrive + t * n_tiles + wk.n_tile, 1) == n_slots - 1;
                     }
                 }
                 // the warp sums its finished rows together: lane l takes columns
@@ -458,16 +540,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (todo) __threadfence();
                 const int n0 = wk.n_tile * BN;
                 const int c = 8 * lane;
-                const int64_t TN = args.T * (int64_t)args.N;
+                const int64_t TN = args.T * (int64_t)N1;
                 while (todo) {
                     const int src_lane = __ffs(todo) - 1;
                     todo &= todo - 1;
                     const int64_t tt = __shfl_sync(0xffffffffu, t, src_lane);
-                    if (n0 + c < args.N) {
-                        const float* src = args.slot + tt * args.N + n0 + c;
+                    if (n0 + c < N1) {
+                        const float* src = slot + tt * N1 + n0 + c;
                         float4 a0 = __ldcg(reinterpret_cast<const float4*>(src));
                         float4 a1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-                        for (int jj = 1; jj < args.n_slots; ++jj) {
+                        for (int jj = 1; jj < n_slots; ++jj) {
                             const float4 b0 = __ldcg(reinterpret_cast<const float4*>(src + jj * TN));
                             const float4 b1 = __ldcg(reinterpret_cast<const float4*>(src + jj * TN + 4));
                             a0.x = a0.x + b0.x; a0.y = a0.y + b0.y; a0.z = a0.z + b0.z; a0.w = a0.w + b0.w;
@@ -482,7 +564,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         o.y = *reinterpret_cast<uint32_t*>(&p1);
                         o.z = *reinterpret_cast<uint32_t*>(&p2);
                         o.w = *reinterpret_cast<uint32_t*>(&p3);
-                        *reinterpret_cast<uint4*>(args.out + tt * args.N + n0 + c) = o;
+                        *reinterpret_cast<uint4*>(out + tt * N1 + n0 + c) = o;
                     }
                 }
             }
@@ -501,24 +583,38 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
 }  // namespace
 
-cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,
-                                const CUtensorMap& tmB1, const GemmArgs& a, int num_sms,
-                                cudaStream_t s)
+cudaError_t launch_grouped_gemm_fused(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,
+                                      const CUtensorMap& tmB1, const CUtensorMap& tmA1,
+                                      const CUtensorMap& tmB2, const GemmArgs& a0, const GemmArgs& a1,
+                                      int num_sms, cudaStream_t s)
 {
-    if (a.M == 0) return cudaSuccess;
-    if (a.G < 1 || a.G > MAX_GROUPS - 1) return cudaErrorInvalidValue;
-    if (a.K % BK != 0) return cudaErrorInvalidValue;
-    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const GemmArgs);
+    if (a0.M == 0) return cudaSuccess;
+    if (a0.G < 1 || a0.G > MAX_GROUPS - 1) return cudaErrorInvalidValue;
+    if (a0.K % BK != 0) return cudaErrorInvalidValue;
+    const bool fused = (mode == kFusedScatter || mode == kFusedCombine);
+    if (fused && (a1.K % BK != 0 || a1.ready == nullptr)) return cudaErrorInvalidValue;
+    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                 const GemmArgs, const GemmArgs);
     if (mode == kGemm0Gather) kern = grouped_gemm_kernel<kGemm0Gather>;
     else if (mode == kGemm0Dense) kern = grouped_gemm_kernel<kGemm0Dense>;
     else if (mode == kGemm1Scatter) kern = grouped_gemm_kernel<kGemm1Scatter>;
     else if (mode == kGemm1Combine) kern = grouped_gemm_kernel<kGemm1Combine>;
     else if (mode == kGemm0CpGather) kern = grouped_gemm_kernel<kGemm0CpGather>;
+    else if (mode == kFusedScatter) kern = grouped_gemm_kernel<kFusedScatter>;
+    else if (mode == kFusedCombine) kern = grouped_gemm_kernel<kFusedCombine>;
     else return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (err != cudaSuccess) return err;
-    kern<<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB0, tmB1, a);
+    kern<<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB0, tmB1, tmA1, tmB2, a0, a1);
     return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,
+                                const CUtensorMap& tmB1, const GemmArgs& a, int num_sms,
+                                cudaStream_t s)
+{
+    if (mode == kFusedScatter || mode == kFusedCombine) return cudaErrorInvalidValue;
+    return launch_grouped_gemm_fused(mode, tmA, tmB0, tmB1, tmB0, tmB0, a, a, num_sms, s);
 }
 
 }  // namespace moe

@@ -66,8 +66,11 @@ cudaError_t launch_tile_table(const int32_t* offsets, int32_t G, int32_t* tile_s
 // of the n_slots contributions to each (token, 256-column tile) (kGemm1Combine).
 // kGemm0CpGather: GEMM0 whose A rows are gathered from x by a producer warp
 // with 16-byte cp.async copies (no x_perm).
+// kFusedScatter / kFusedCombine: GEMM0 (dense A) and GEMM1 (scatter / combine)
+// in one persistent launch; a GEMM1 tile waits (bounded) until the GEMM0 tiles
+// of its (expert, M tile) have published their rows of h.
 enum GemmMode { kGemm0Gather = 0, kGemm1Scatter = 1, kGemm0Dense = 2, kGemm1Combine = 3,
-                kGemm0CpGather = 4 };
+                kGemm0CpGather = 4, kFusedScatter = 5, kFusedCombine = 6 };
 
 struct GemmArgs {
     int32_t M;                   // rows in dispatched order (R, or T for a dense expert)
@@ -87,6 +90,8 @@ struct GemmArgs {
     int32_t n_slots;             // kGemm1Combine: contributions summed per (token, N tile)
     int32_t* arrive;             // kGemm1Combine: [T, ceil(N/256)] tickets, zero before the first launch
     uint16_t* out;               // kGemm1Combine: [T, N] bf16 layer output
+    int32_t* ready;              // fused, GEMM1 args: [M tiles] count of GEMM0 warps done, zero first
+    int32_t ready_target;        // fused, GEMM1 args: count that makes an M tile's h complete
     uint32_t* err;
 };
 
@@ -98,6 +103,12 @@ struct GemmArgs {
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,
                                 const CUtensorMap& tmB1, const GemmArgs& a, int num_sms,
                                 cudaStream_t s);
+// Both GEMMs in one launch: a0 / tmA, tmB0, tmB1 as for kGemm0Dense; a1 / tmA1
+// (h) and tmB2 (W2) as for GEMM1. mode is kFusedScatter or kFusedCombine.
+cudaError_t launch_grouped_gemm_fused(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,
+                                      const CUtensorMap& tmB1, const CUtensorMap& tmA1,
+                                      const CUtensorMap& tmB2, const GemmArgs& a0, const GemmArgs& a1,
+                                      int num_sms, cudaStream_t s);
 
 cudaError_t launch_combine(const float* slot, int32_t n_slots, uint16_t* out, int64_t T, int32_t H,
                            int num_sms, cudaStream_t s);

@@ -32,6 +32,10 @@ OPT_COMBINE = 1
 COMBINE_AUTO = 0          # fused when the last GEMM1 has K >= 4096
 COMBINE_FUSED = 1         # GEMM1's epilogue: the last contribution sums the slots
 COMBINE_SEPARATE = 2      # a streaming combine kernel after the GEMMs
+OPT_GEMM_FUSION = 2
+GEMM_FUSION_AUTO = 0      # by shape (the library's table)
+GEMM_FUSION_ON = 1        # both routed GEMMs in one persistent launch
+GEMM_FUSION_OFF = 2       # two launches
 
 
 class MoeError(RuntimeError):
@@ -138,6 +142,15 @@ def set_combine(mode: int) -> None:
 
 def get_combine() -> int:
     return int(load().moe_get_option(OPT_COMBINE))
+
+
+def set_gemm_fusion(mode: int) -> None:
+    """Run the routed GEMMs as one launch or two (GEMM_FUSION_AUTO / _ON / _OFF)."""
+    _ok(load().moe_set_option(OPT_GEMM_FUSION, int(mode)), "moe_set_option")
+
+
+def get_gemm_fusion() -> int:
+    return int(load().moe_get_option(OPT_GEMM_FUSION))
 
 
 def make_dims(T, H, F, E, k, F_shared=0) -> Dims:
