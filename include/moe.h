@@ -157,6 +157,34 @@ moe_status moe_set_option(int option, int value);
 /* Current value of an option, or -1 for an unknown option. */
 int moe_get_option(int option);
 
+/* Router kernels (moe_plan.router). All compute the same logits bit for bit. */
+enum {
+    MOE_ROUTER_STREAM = 0,   /* E <= 8: TMA-fed per-warp pipelines, top-k fused */
+    MOE_ROUTER_SLICED = 1,   /* E > 8, a multiple of 8, inside moe_layer_forward: expert
+                              * slices of 8 per CTA, logits to the workspace, top-k pass */
+    MOE_ROUTER_CLUSTER = 2,  /* 8 < E <= 64: canonical lanes split over a CTA cluster */
+    MOE_ROUTER_BLOCK = 3     /* anything else: one CTA per SM, gate staged in slices */
+};
+
+/* The configuration moe_layer_forward runs for a shape under the current
+ * options: the library's per-shape table, fixed before any launch. */
+typedef struct {
+    int32_t router;        /* MOE_ROUTER_* */
+    int32_t gemm0_a;       /* MOE_GEMM0_A_* in effect */
+    int32_t combine;       /* MOE_COMBINE_FUSED or MOE_COMBINE_SEPARATE */
+    int32_t gemm_fusion;   /* MOE_GEMM_FUSION_ON or MOE_GEMM_FUSION_OFF */
+    int32_t tile_m;        /* grouped GEMM tile rows (routed rows per tile) */
+    int32_t tile_n;        /* grouped GEMM MMA N (GEMM0: half W1, half W3) */
+    int32_t tile_k;        /* K per pipeline stage */
+    int32_t stages;        /* shared-memory pipeline stages */
+    int32_t cta_group;     /* CTAs per MMA (tcgen05 cta_group) */
+} moe_plan;
+
+/* Fills *plan for `dims` (host only: no device work, no launch). Returns
+ * MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED for shapes moe_layer_forward
+ * rejects. */
+moe_status moe_layer_plan(const moe_dims* dims, moe_plan* plan);
+
 /* Library version (major*10000 + minor*100 + patch). */
 int moe_version(void);
 

@@ -114,3 +114,46 @@ def test_zero_tokens_is_noop_on_host(L):
     d = lib.make_dims(0, 64, 64, 8, 2)
     assert L.moe_route(ctypes.byref(d), None, None, None, None, None, None) == 0
     assert L.moe_combine(ctypes.byref(d), None, 1, None, None) == 0
+
+
+def test_layer_plan_table(L):
+    """The per-shape table: router, combine form and GEMM fusion chosen for the
+    layer configurations (host only), and the options that override it."""
+    from token_dispatch_grouped_moe_gb300 import lib
+    from token_dispatch_grouped_moe_gb300.configs import CONFIGS
+    want = {   # config: (router, combine, gemm_fusion)
+        "tiny": (lib.ROUTER_STREAM, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON),
+        "mixtral": (lib.ROUTER_STREAM, lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF),
+        "qwen2": (lib.ROUTER_SLICED, lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF),
+        "dsk-1k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON),
+        "dsk-4k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON),
+        "dsk-32k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_OFF),
+    }
+    for name, (router, combine, fusion) in want.items():
+        c = CONFIGS[name]
+        p = lib.layer_plan(lib.make_dims(c.T, c.H, c.F, c.E, c.k, c.Fs))
+        assert (p.router, p.combine, p.gemm_fusion) == (router, combine, fusion), name
+        assert (p.gemm0_a, p.tile_m, p.tile_n, p.tile_k, p.stages, p.cta_group) == (
+            lib.GEMM0_A_PERMUTED, 128, 256, 64, 4, 1)
+    # E not a multiple of 8, E > 64, a gate too large for the streaming router
+    assert lib.layer_plan(lib.make_dims(64, 256, 64, 12, 2)).router == lib.ROUTER_CLUSTER
+    assert lib.layer_plan(lib.make_dims(64, 256, 64, 200, 2)).router == lib.ROUTER_SLICED
+    assert lib.layer_plan(lib.make_dims(64, 256, 64, 196, 2)).router == lib.ROUTER_BLOCK
+    assert lib.layer_plan(lib.make_dims(64, 16384, 64, 8, 2)).router == lib.ROUTER_BLOCK
+    # options override the automatic entries; a gather A path rules out fusion
+    d = lib.make_dims(1024, 2048, 1408, 64, 6)
+    try:
+        lib.set_combine(lib.COMBINE_FUSED)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_OFF)
+        p = lib.layer_plan(d)
+        assert (p.combine, p.gemm_fusion) == (lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_ON)
+        lib.set_gemm0_a(lib.GEMM0_A_TMA_GATHER)
+        assert lib.layer_plan(d).gemm_fusion == lib.GEMM_FUSION_OFF
+    finally:
+        lib.set_combine(lib.COMBINE_AUTO)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
+        lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
+    with pytest.raises(lib.MoeError):
+        lib.layer_plan(lib.make_dims(64, 100, 64, 8, 2))   # H not a multiple of 64
+

@@ -96,15 +96,41 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t oute
     return encode_map_2d(m, base, inner, outer, 64, box_outer, true);
 }
 
-// The shapes for which one launch of both routed GEMMs measured faster than
-// two (MOE_GEMM_FUSION_AUTO): fewer than 512 routed rows per expert on
-// average, where the GEMMs are short (a few waves of tiles, weight-bandwidth
-// bound) and the GEMM0 tail and launch boundary weigh (DeepSeek-shaped T=1024:
-// 0.273 -> 0.259 ms per layer, T=4096: 0.484 -> 0.468 ms). From 512 rows per
-// expert up (Qwen2, DeepSeek T=32768, Mixtral) the two forms measured the same.
-bool auto_fuse_gemms(const moe_dims& d)
+// The per-shape table of moe_layer_forward (all entries measured on GB300):
+//  - router: by E and the gate's shared-memory size (route_variant);
+//  - combine, automatic: fused into GEMM1's epilogue when the last GEMM1 to
+//    run has K >= 4096 (Mixtral F = 14336, Qwen2 shared F = 20480), where the
+//    epilogue work hides behind a long main loop; separate for short tiles
+//    (DeepSeek F = 1408: fused GEMM1 0.42 -> 0.81 ms at T = 16384, k = 6);
+//  - GEMM fusion, automatic: both routed GEMMs in one launch below 512 routed
+//    rows per expert on average, where the GEMMs are short and
+//    weight-bandwidth bound and the GEMM0 tail and launch boundary weigh
+//    (DeepSeek-shaped T = 1024: 0.273 -> 0.259 ms per layer, T = 4096:
+//    0.484 -> 0.467 ms); from 512 rows per expert up (Qwen2, DeepSeek
+//    T = 32768, Mixtral) the two forms measured the same;
+//  - one compiled GEMM tile: 128 x 256 x 64, 4 stages, one CTA per MMA. Zipf
+//    routing needs no reordering: the static schedule spreads every expert's
+//    tiles over all SMs (Mixtral-Zipf measured as fast as uniform routing).
+moe_plan plan_of(const moe_dims& d)
 {
-    return d.T * (int64_t)d.k < (int64_t)512 * d.E;
+    moe_plan p{};
+    p.router = route_variant(d.H, d.E, /*has_logits=*/true);
+    p.gemm0_a = g_gemm0_a.load();
+    const int combine_opt = g_combine.load();
+    const int32_t k_last = d.F_shared > 0 ? d.F_shared : d.F;
+    p.combine = (combine_opt == MOE_COMBINE_FUSED || (combine_opt == MOE_COMBINE_AUTO && k_last >= 4096))
+                    ? MOE_COMBINE_FUSED : MOE_COMBINE_SEPARATE;
+    const int fusion_opt = g_gemm_fusion.load();
+    const bool fuse = p.gemm0_a == MOE_GEMM0_A_PERMUTED &&
+                      (fusion_opt == MOE_GEMM_FUSION_ON ||
+                       (fusion_opt == MOE_GEMM_FUSION_AUTO && d.T * (int64_t)d.k < (int64_t)512 * d.E));
+    p.gemm_fusion = fuse ? MOE_GEMM_FUSION_ON : MOE_GEMM_FUSION_OFF;
+    p.tile_m = kTileM;
+    p.tile_n = 256;
+    p.tile_k = 64;
+    p.stages = 4;
+    p.cta_group = 1;
+    return p;
 }
 
 // ------------------------------------------------------------ workspace --
@@ -337,6 +363,14 @@ int moe_get_option(int option)
     return -1;
 }
 
+moe_status moe_layer_plan(const moe_dims* dims, moe_plan* plan)
+{
+    MOE_TRY_STATUS(check_dims(dims));
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    *plan = plan_of(*dims);
+    return MOE_OK;
+}
+
 size_t moe_workspace_size(const moe_dims* dims)
 {
     if (check_dims(dims) != MOE_OK) return 0;
@@ -510,12 +544,8 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     const int64_t R = d.T * d.k;
     const int32_t n_slots = d.k + (d.F_shared > 0 ? 1 : 0);
     int32_t* arrive = reinterpret_cast<int32_t*>(w + L.arrive);
-    // Fused combine: measured faster when the last GEMM1's K loop is long
-    // (Mixtral F = 14336, Qwen2 shared F = 20480), slower for short tiles
-    // (DeepSeek F = 1408), where the epilogue is already the bottleneck.
-    const int combine_opt = g_combine.load();
-    const int32_t k_last = d.F_shared > 0 ? d.F_shared : d.F;
-    const bool fused = combine_opt == MOE_COMBINE_FUSED || (combine_opt == MOE_COMBINE_AUTO && k_last >= 4096);
+    const moe_plan plan = plan_of(d);
+    const bool fused = plan.combine == MOE_COMBINE_FUSED;
     if (fused)   // GEMM1 counts contributions per (token, 256-column tile)
         MOE_TRY(cudaMemsetAsync(arrive, 0, (size_t)d.T * ((d.H + 255) / 256) * 4, s));
 
@@ -531,17 +561,14 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                    R, d.E};
     MOE_TRY(launch_permute(pa, s));
 
-    const int a_opt = g_gemm0_a.load();
-    const bool permuted = (a_opt == MOE_GEMM0_A_PERMUTED);
-    const bool cp_gather = (a_opt == MOE_GEMM0_A_CP_GATHER);
+    const bool permuted = (plan.gemm0_a == MOE_GEMM0_A_PERMUTED);
+    const bool cp_gather = (plan.gemm0_a == MOE_GEMM0_A_CP_GATHER);
     uint16_t* xp = reinterpret_cast<uint16_t*>(w + L.xp);
     if (permuted)
         MOE_TRY(launch_gather_rows(x, src, offsets + d.E, xp, R, d.T, d.H, d.k, err, sms, s));
 
     // both routed GEMMs in one launch (dense A only)
-    const int fusion_opt = g_gemm_fusion.load();
-    const bool fuse_gemms = permuted && (fusion_opt == MOE_GEMM_FUSION_ON ||
-                                         (fusion_opt == MOE_GEMM_FUSION_AUTO && auto_fuse_gemms(d)));
+    const bool fuse_gemms = plan.gemm_fusion == MOE_GEMM_FUSION_ON;
 
     record(events ? events->before_gemm0 : nullptr, s);
     MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)R, d.F, d.E, d.k, x, permuted ? xp : nullptr, src,

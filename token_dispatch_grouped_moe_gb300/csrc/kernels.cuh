@@ -25,6 +25,9 @@ struct RouteArgs {
     float* logits = nullptr;   // [T,E] fp32 scratch for E > 8 (the sliced router), or null
 };
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s);
+// The router kernel launch_route runs for these sizes (MOE_ROUTER_*);
+// has_logits: a [T,E] logits scratch is passed (the layer call).
+int route_variant(int32_t H, int32_t E, bool has_logits);
 
 // A TMA tensor map of a row-major bf16 matrix [outer, inner] with box
 // {box_inner, box_outer}, 128-byte swizzle or none; out-of-bounds elements

@@ -47,6 +47,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "../../include/moe.h"
 #include "kernels.cuh"
 #include "ptx.cuh"
 
@@ -1120,31 +1121,53 @@ bool launch_stream(const RouteArgs& a, int num_sms, cudaStream_t s, cudaError_t&
 
 }  // namespace
 
+namespace {
+
+constexpr size_t kStreamBudget = 227 * 1024;
+// Twelve warps: the mixed-precision FMA needs more than two warps per
+// scheduler to approach its issue rate (measured: 8 -> 12 warps,
+// DeepSeek-shaped 244 -> 232 us; E = 8 unchanged).
+using StreamShape = SShape<8, 3, 12>;
+
+// Whether some cluster shape of this expert bucket fits shared memory (the
+// smallest one: a cluster of 8 with a bf16 gate).
+bool cluster_fits(int32_t H, int32_t E)
+{
+    if (E <= 8 || E > 64) return false;
+    // the shapes launch_cluster_any tries for each bucket, at CS = 8, bf16 gate
+    if (E <= 16) return CShape<8, 16, 1, 2, false, 1>::smem_bytes(H, E) <= kSmemBudget;
+    if (E <= 32) return CShape<8, 16, 2, 4, false, 1>::smem_bytes(H, E) <= kSmemBudget;
+    return CShape<8, 16, 4, 4, false, 1>::smem_bytes(H, E) <= kSmemBudget;
+}
+
+}  // namespace
+
+int route_variant(int32_t H, int32_t E, bool has_logits)
+{
+    const bool stream_fits = StreamShape::smem_bytes(H) <= kStreamBudget;
+    if (E <= 8 && stream_fits) return MOE_ROUTER_STREAM;
+    if (E > 8 && has_logits && E % 8 == 0 && stream_fits) return MOE_ROUTER_SLICED;
+    if (cluster_fits(H, E)) return MOE_ROUTER_CLUSTER;
+    return MOE_ROUTER_BLOCK;
+}
+
 cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s)
 {
     if (a.T == 0) return cudaSuccess;
-    bool launched = false;
     cudaError_t err = cudaSuccess;
-    // E <= 8: the streaming router while its gate fits shared memory. Twelve
-    // warps: the mixed-precision FMA needs more than two warps per scheduler
-    // to approach its issue rate (measured: 8 -> 12 warps, DeepSeek-shaped
-    // 244 -> 232 us; E = 8 unchanged)
-    constexpr size_t kStreamBudget = 227 * 1024;
-    if (a.E <= 8) {
-        if (SShape<8, 3, 12>::smem_bytes(a.H) <= kStreamBudget && launch_stream<SShape<8, 3, 12>>(a, num_sms, s, err))
-            return err;
-    } else if (a.logits && a.E % 8 == 0 && SShape<8, 3, 12>::smem_bytes(a.H) <= kStreamBudget &&
-               launch_stream<SShape<8, 3, 12>>(a, num_sms, s, err)) {
-        // E > 8 with room for the logits: expert slices plus a top-k pass
+    const int variant = route_variant(a.H, a.E, a.logits != nullptr);
+    // (launch_stream returns false only if a tensor map cannot be encoded;
+    // then the block router below runs)
+    if ((variant == MOE_ROUTER_STREAM || variant == MOE_ROUTER_SLICED) &&
+        launch_stream<StreamShape>(a, num_sms, s, err))
         return err;
-    } else if (a.E <= 16)
-        err = launch_cluster_any<16, 1, 2, 1, 2>(a, num_sms, s, launched);
-    else if (a.E <= 32)
-        err = launch_cluster_any<16, 2, 4, 1, 2>(a, num_sms, s, launched);
-    else if (a.E <= 64)
-        err = launch_cluster_any<16, 4, 4, 1, 2>(a, num_sms, s, launched);
-    if (launched) return err;
-    // more than 64 experts, or a gate too large for a cluster of 8
+    if (variant == MOE_ROUTER_CLUSTER) {
+        bool launched = false;
+        if (a.E <= 16) err = launch_cluster_any<16, 1, 2, 1, 2>(a, num_sms, s, launched);
+        else if (a.E <= 32) err = launch_cluster_any<16, 2, 4, 1, 2>(a, num_sms, s, launched);
+        else err = launch_cluster_any<16, 4, 4, 1, 2>(a, num_sms, s, launched);
+        if (launched) return err;
+    }
     if (a.E <= 8) return launch_route_t<8, 4>(a, num_sms, s);
     if (a.E <= 16) return launch_route_t<16, 2>(a, num_sms, s);
     if (a.E <= 32) return launch_route_t<32, 2>(a, num_sms, s);

@@ -22,7 +22,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 
 EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_set_option",
-           "moe_get_option", "moe_permute_static", "moe_route_ex", "moe_layer_forward_ex"]
+           "moe_get_option", "moe_permute_static", "moe_route_ex", "moe_layer_forward_ex",
+           "moe_layer_plan"]
 
 OPT_GEMM0_A = 0
 GEMM0_A_PERMUTED = 0      # dispatch copies token rows to x_perm; GEMM0 loads dense tiles
@@ -62,6 +63,14 @@ class Gating(ctypes.Structure):
 class RoutingOut(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("topk_idx", "topk_w", "counts", "offsets", "src_row",
                                                "inv_pos")]
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("router", "gemm0_a", "combine", "gemm_fusion", "tile_m",
+                                              "tile_n", "tile_k", "stages", "cta_group")]
+
+
+ROUTER_STREAM, ROUTER_SLICED, ROUTER_CLUSTER, ROUTER_BLOCK = 0, 1, 2, 3
 
 
 _lib = None
@@ -105,6 +114,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_forward_ex.restype = ctypes.c_int
     lib.moe_layer_forward_ex.argtypes = [D, P, P, P, ctypes.POINTER(Gating), P, P, P, P, P, P, P,
                                          ctypes.POINTER(RoutingOut), P, sz, ctypes.POINTER(StageEvents), P]
+    lib.moe_layer_plan.restype = ctypes.c_int
+    lib.moe_layer_plan.argtypes = [D, ctypes.POINTER(Plan)]
     lib.moe_layer_forward.restype = ctypes.c_int
     lib.moe_layer_forward.argtypes = [D, P, P, P, P, P, P, P, P, P, P, ctypes.POINTER(RoutingOut), P,
                                       sz, ctypes.POINTER(StageEvents), P]
@@ -151,6 +162,13 @@ def set_gemm_fusion(mode: int) -> None:
 
 def get_gemm_fusion() -> int:
     return int(load().moe_get_option(OPT_GEMM_FUSION))
+
+
+def layer_plan(dims: Dims) -> Plan:
+    """The configuration moe_layer_forward runs for this shape (host only)."""
+    p = Plan()
+    _ok(load().moe_layer_plan(ctypes.byref(dims), ctypes.byref(p)), "moe_layer_plan")
+    return p
 
 
 def make_dims(T, H, F, E, k, F_shared=0) -> Dims:
