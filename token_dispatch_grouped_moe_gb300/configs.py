@@ -47,4 +47,7 @@ CONFIGS = {
     # Mixtral-shaped with T and F quartered: small enough (0.7 GB of weights)
     # for multi-pass profiler captures, still larger than L2.
     "mixtral-prof": LayerConfig("mixtral-prof", T=2048, H=4096, F=3584, E=8, k=2),
+    # Qwen2-shaped routed experts (H, F, k, 512 rows per expert) with 16 experts
+    # and no shared expert: 0.9 GB of weights, for multi-pass profiler captures.
+    "qwen2-prof": LayerConfig("qwen2-prof", T=1024, H=3584, F=2560, E=16, k=8),
 }

@@ -72,7 +72,7 @@ EncodeTiledFn encode_fn()
 }  // namespace
 
 bool encode_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                   uint32_t box_outer, bool swizzle_128)
+                   uint32_t box_outer, int swizzle_bytes)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
@@ -82,18 +82,26 @@ bool encode_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t ou
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    swizzle_128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    swizzle_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                    : swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                          : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 namespace {
 
-// 2D bf16 tensor [outer, inner] (inner contiguous), box {64, box_outer},
-// 128-byte swizzle; out-of-bounds elements read as zero.
-bool make_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_outer)
+// The grouped GEMM's operands, bf16 [outer, inner] (inner contiguous);
+// out-of-bounds elements read as zero.
+// A (K-major rows): box {kGemmBK, box_rows}, swizzle = one A row (kGemmBK * 2 bytes).
+bool make_map_a(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_rows)
 {
-    return encode_map_2d(m, base, inner, outer, 64, box_outer, true);
+    return encode_map_2d(m, base, inner, outer, kGemmBK, box_rows, kGemmBK * 2);
+}
+// B (weights, N contiguous): box {64 columns, kGemmBK k-rows}, 128-byte swizzle.
+bool make_map_b(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer)
+{
+    return encode_map_2d(m, base, inner, outer, 64, kGemmBK, 128);
 }
 
 // The per-shape table of moe_layer_forward (all entries measured on GB300):
@@ -244,13 +252,13 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
     }
     CUtensorMap mx, m1, m3, mh, m2;
     const bool dense = (x_rows != nullptr);
-    const bool ok_a = dense ? make_map_2d(&mx, x_rows, (uint64_t)d.H, (uint64_t)M, 128)
-                            : make_map_2d(&mx, x, (uint64_t)d.H, (uint64_t)d.T, 1);
+    const bool ok_a = dense ? make_map_a(&mx, x_rows, (uint64_t)d.H, (uint64_t)M, 128)
+                            : make_map_a(&mx, x, (uint64_t)d.H, (uint64_t)d.T, 1);
     if (!ok_a ||
-        !make_map_2d(&m1, W1, (uint64_t)F, (uint64_t)G * d.H, 64) ||
-        !make_map_2d(&m3, W3, (uint64_t)F, (uint64_t)G * d.H, 64) ||
-        !make_map_2d(&mh, h, (uint64_t)F, (uint64_t)M, 128) ||
-        !make_map_2d(&m2, W2, (uint64_t)d.H, (uint64_t)G * F, 64))
+        !make_map_b(&m1, W1, (uint64_t)F, (uint64_t)G * d.H) ||
+        !make_map_b(&m3, W3, (uint64_t)F, (uint64_t)G * d.H) ||
+        !make_map_a(&mh, h, (uint64_t)F, (uint64_t)M, 128) ||
+        !make_map_b(&m2, W2, (uint64_t)d.H, (uint64_t)G * F))
         return MOE_ERR_CUDA;
     GemmArgs a{};
     a.M = M;

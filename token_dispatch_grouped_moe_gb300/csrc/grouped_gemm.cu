@@ -63,12 +63,14 @@ namespace {
 
 constexpr int BM = kTileM;   // 128
 constexpr int BN = 256;      // MMA N (GEMM0: 128 of W1 + 128 of W3)
-constexpr int BK = 64;       // 64 bf16 = one 128-byte swizzle row
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;         // 16 KB
-constexpr int B_BYTES = BN * BK * 2;         // 32 KB
+constexpr int BK = kGemmBK;  // K per stage: one A row of BK bf16 = one swizzle span
+constexpr int A_ROW = BK * 2;                // bytes: 64 (64-byte swizzle) or 128 (128-byte)
+constexpr int STAGES = BK == 32 ? 9 : 4;     // 9 x 24 KB or 4 x 48 KB of shared memory
+static_assert(BK == 32 || BK == 64, "A rows are one 64- or 128-byte swizzle span");
+constexpr int A_BYTES = BM * BK * 2;         // 8 KB (BK 32) or 16 KB
+constexpr int B_BYTES = BN * BK * 2;         // 16 KB (BK 32) or 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int B_CHUNK_BYTES = BK * 128;      // one 64-column slice of B: 64 k-rows x 128 B
+constexpr int B_CHUNK_BYTES = BK * 128;      // one 64-column slice of B: BK k-rows x 128 B
 constexpr int NUM_THREADS = 224;   // 7 warps: TMA, MMA, 4 x epilogue, row gather
 constexpr int GATHER_LAG = 2;      // stages a gathered A tile is given to land
 constexpr int MAX_GROUPS = 257;
@@ -274,7 +276,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (lane == 0) mbar_arrive_expect_tx(full, CP_GATHER ? B_BYTES : STAGE_BYTES);
                 __syncwarp();
                 if (GATHER)
-                    tma_gather4(a_dst + lane * 512, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], full);
+                    tma_gather4(a_dst + lane * 4 * A_ROW, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], full);
                 else if (!CP_GATHER && lane == 0)
                     tma_load_2d(a_dst, p1 ? &tmA1 : &tmA, kb * BK, wk.row0, full);
                 if (HAS_GEMM0 && !p1) {
@@ -334,7 +336,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+                        // K-major A: each K step of 16 is 32 bytes further along the row
+                        const uint64_t ad = BK == 64 ? smem_desc_sw128(a_base + kk * 32, 16, 1024)
+                                                     : smem_desc_sw64(a_base + kk * 32, 16, 512);
                         const uint64_t bd = smem_desc_sw128(b_base + kk * 16 * 128, B_CHUNK_BYTES, 1024);
                         tc_mma_f16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
@@ -360,8 +364,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             uint32_t phase = 0;
             int pending = 0;   // stages issued whose rows are not yet published
             bool ok = true;
-            const int c = lane & 7;        // 16-byte chunk of a 128-byte row
-            const int rsub = lane >> 3;    // row within a group of four
+            constexpr int CPR = A_ROW / 16;   // 16-byte chunks per A row (4 or 8)
+            const int c = lane % CPR;         // this lane's chunk of a row
+            const int rsub = lane / CPR;      // row within a group of 32 / CPR
             auto publish_oldest = [&]() {
                 // the oldest pending stage's copies have landed (this lane's): make
                 // them visible to the tensor cores, then arrive once for the warp
@@ -396,10 +401,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t a_dst = tiles_addr + stage * STAGE_BYTES;
                     const uint16_t* xk = args.x + kb * BK + c * 8;
 #pragma unroll 8
-                    for (int q = 0; q < BM / 4; ++q) {
-                        const int r = 4 * q + rsub;
+                    for (int q = 0; q < BM / (32 / CPR); ++q) {
+                        const int r = (32 / CPR) * q + rsub;
                         const uint16_t* src = xk + (int64_t)st->tok[r] * args.K;
-                        const uint32_t dst = a_dst + r * 128 + ((c ^ (r & 7)) << 4);
+                        // the swizzle of the TMA / tensor-core layout: 16-byte chunk
+                        // index XOR row bits (128-byte rows: r mod 8; 64-byte: (r/2) mod 4)
+                        const int swz = BK == 64 ? (r & 7) : ((r >> 1) & 3);
+                        const uint32_t dst = a_dst + r * A_ROW + ((c ^ swz) << 4);
                         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src)
                                      : "memory");
                     }

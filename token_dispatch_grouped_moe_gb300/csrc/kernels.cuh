@@ -11,6 +11,11 @@
 namespace moe {
 
 constexpr int kTileM = 128;   // GEMM M tile (routed rows per tile)
+// GEMM K per pipeline stage: 64 bf16 (128-byte A rows, 128-byte swizzle, 4
+// stages of 48 KB) or 32 (64-byte rows, 64-byte swizzle, 9 stages of 24 KB).
+// 32 keeps more bytes in flight per SM but measured half the throughput
+// (Mixtral-shaped layer 3.46 -> 5.92 ms), so 64.
+constexpr int kGemmBK = 64;
 
 struct RouteArgs {
     const uint16_t* x;     // [T,H] bf16 bits
@@ -30,10 +35,11 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s);
 int route_variant(int32_t H, int32_t E, bool has_logits);
 
 // A TMA tensor map of a row-major bf16 matrix [outer, inner] with box
-// {box_inner, box_outer}, 128-byte swizzle or none; out-of-bounds elements
+// {box_inner, box_outer}, a 128- or 64-byte swizzle or none (swizzle_bytes
+// 128, 64 or 0); out-of-bounds elements
 // read as zero. False if the driver entry point or the encoding fails.
 bool encode_map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint32_t box_inner,
-                   uint32_t box_outer, bool swizzle_128);
+                   uint32_t box_outer, int swizzle_bytes);
 
 // scale[t] = 1 / (1 + exp(-x[t] . wsg)) (the shared expert's sigmoid gate)
 cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* wsg, float* scale, int64_t T,

@@ -256,6 +256,18 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
 //   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format
 //   (1 = bf16); 15 A major (0 = K); 16 B major (1 = MN); 17-22 N >> 3;
 //   24-28 M >> 4.
+// The same for a K-major operand in 64-byte-swizzled rows (layout type 4):
+// 8-row groups sbo bytes apart (512 for dense 64-byte rows).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)4 << 61;
+    return d;
+}
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn_major,
                                                       bool b_mn_major)
 {

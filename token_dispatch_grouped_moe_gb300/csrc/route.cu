@@ -1090,9 +1090,9 @@ bool launch_stream(const RouteArgs& a, int num_sms, cudaStream_t s, cudaError_t&
     CUtensorMap gmap, xmap;
     std::memset(&gmap, 0, sizeof(gmap));
     // x as a bf16 [T, H] matrix, box {256, NT}: one step of NT token rows
-    if (!encode_map_2d(&xmap, a.x, (uint64_t)a.H, (uint64_t)a.T, 256, S::NT, false)) return false;
+    if (!encode_map_2d(&xmap, a.x, (uint64_t)a.H, (uint64_t)a.T, 256, S::NT, 0)) return false;
     // the gate Wg[H, 8] as a bf16 [H/8, 64] matrix, box {64, 32}, 128-byte swizzle
-    const bool gate_tma = a.E == 8 && encode_map_2d(&gmap, a.Wg, 64, (uint64_t)a.H / 8, 64, 32, true);
+    const bool gate_tma = a.E == 8 && encode_map_2d(&gmap, a.Wg, 64, (uint64_t)a.H / 8, 64, 32, 128);
     const size_t smem = S::smem_bytes(a.H);
     auto kern = route_stream_kernel<S>;
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
