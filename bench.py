@@ -49,6 +49,18 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest value over the ranks of the process group (the value itself
+    on one rank): each rank times its own replica, the job takes the slowest."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -240,11 +252,7 @@ def bench_ours(args, cfg):
         step_ms.append(t[-1])
         for j, n in enumerate(stage_ms):
             stage_ms[n].append(t[j + 1] - t[j])
-    ms = float(np.sum(step_ms)) / args.steps
-    if world > 1:
-        tt = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(float(np.sum(step_ms)) / args.steps, device)
 
     # end to end through the C ABI with host buffers: x H2D, layer, out D2H
     x_host = inp["x"].pin_memory()
@@ -263,11 +271,7 @@ def bench_ours(args, cfg):
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
-    e2e = float(np.mean(e2e_ms))
-    if world > 1:
-        tt = torch.tensor([e2e], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e = float(tt.item())
+    e2e = max_over_ranks(float(np.mean(e2e_ms)), device)
 
     if rank != 0:
         if world > 1:
