@@ -185,6 +185,14 @@ typedef struct {
  * rejects. */
 moe_status moe_layer_plan(const moe_dims* dims, moe_plan* plan);
 
+/* Self-test of the failure path every pipeline wait takes: one device thread
+ * waits, bounded by limit_ms (1..4000) of %globaltimer time, on a device flag
+ * that nothing sets, gives up, and reports it through a device error word.
+ * Returns MOE_ERR_TIMEOUT when that happened (the expected outcome), MOE_OK if
+ * the wait somehow completed, MOE_ERR_CUDA on a launch or copy error. The
+ * device stays usable. Synchronises `stream`. */
+moe_status moe_selftest_wait_timeout(int32_t limit_ms, moe_stream_t stream);
+
 /* Library version (major*10000 + minor*100 + patch). */
 int moe_version(void);
 

@@ -6,6 +6,8 @@ the oracle's fp64 output: max |out - ref| <= 2e-2 * rms(ref).
 """
 import os
 
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -496,6 +498,17 @@ def test_bad_expert_id_reported(lib):
     assert int(counts.sum()) == T * k - 2
     g = guard.cpu().numpy()
     assert np.all(g[:32] == -7) and np.all(g[32 + T * k:] == -7)
+
+
+def test_bounded_wait_times_out(lib, oracle):
+    """A device wait on a flag that nothing sets gives up after its limit,
+    reports MOE_ERR_TIMEOUT through the device error word, and leaves the
+    context usable: a layer call right after it is still correct."""
+    t0 = time.time()
+    assert lib.selftest_wait_timeout(300) == lib.MOE_ERR_TIMEOUT
+    assert 0.25 < time.time() - t0 < 30.0
+    T, H, F, E, k, Fs = SMALL_CASES["tiny"]
+    run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=4, tol="elementwise")
 
 
 def test_zero_tokens(lib):

@@ -115,33 +115,6 @@ __device__ __forceinline__ Work decode_work(int w, int n_tiles, const int* ts, c
     return r;
 }
 
-// Waits until *ctr >= target (acquire, GPU scope). Returns false (after
-// recording a timeout and raising *abort) if that takes longer than
-// kWaitLimitNs of %globaltimer time or another role has aborted.
-__device__ __forceinline__ bool wait_count(const int32_t* ctr, int32_t target, volatile int* abort,
-                                           uint32_t* err)
-{
-    auto load = [&]() {
-        int32_t v;
-        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-        return v;
-    };
-    if (load() >= target) return true;
-    const unsigned long long t0 = globaltimer_ns();
-    for (uint32_t i = 1;; ++i) {
-        __nanosleep(128);
-        if (load() >= target) return true;
-        if ((i & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                *abort = 1;
-                report_error(err, MOE_DEV_ERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,

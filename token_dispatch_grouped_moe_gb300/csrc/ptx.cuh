@@ -119,6 +119,33 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity)
     }
 }
 
+// Waits until *ctr >= target (acquire, GPU scope). Returns false (after
+// recording a timeout and raising *abort) if that takes longer than limit_ns
+// of %globaltimer time or another role has aborted.
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int32_t target, volatile int* abort,
+                                           uint32_t* err, unsigned long long limit_ns = kWaitLimitNs)
+{
+    auto load = [&]() {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        return v;
+    };
+    if (load() >= target) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        __nanosleep(128);
+        if (load() >= target) return true;
+        if ((i & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) {
+                *abort = 1;
+                report_error(err, MOE_DEV_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------------ TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap)

@@ -17,13 +17,14 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmoe_gb300.so")
 
 MOE_OK = 0
+MOE_ERR_TIMEOUT = 5
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE_BOUNDS"}
 
 EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_set_option",
            "moe_get_option", "moe_permute_static", "moe_route_ex", "moe_layer_forward_ex",
-           "moe_layer_plan"]
+           "moe_layer_plan", "moe_selftest_wait_timeout"]
 
 OPT_GEMM0_A = 0
 GEMM0_A_PERMUTED = 0      # dispatch copies token rows to x_perm; GEMM0 loads dense tiles
@@ -114,6 +115,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_forward_ex.restype = ctypes.c_int
     lib.moe_layer_forward_ex.argtypes = [D, P, P, P, ctypes.POINTER(Gating), P, P, P, P, P, P, P,
                                          ctypes.POINTER(RoutingOut), P, sz, ctypes.POINTER(StageEvents), P]
+    lib.moe_selftest_wait_timeout.restype = ctypes.c_int
+    lib.moe_selftest_wait_timeout.argtypes = [i32, P]
     lib.moe_layer_plan.restype = ctypes.c_int
     lib.moe_layer_plan.argtypes = [D, ctypes.POINTER(Plan)]
     lib.moe_layer_forward.restype = ctypes.c_int
@@ -162,6 +165,11 @@ def set_gemm_fusion(mode: int) -> None:
 
 def get_gemm_fusion() -> int:
     return int(load().moe_get_option(OPT_GEMM_FUSION))
+
+
+def selftest_wait_timeout(limit_ms: int = 200, stream=None) -> int:
+    """Status of the bounded-wait self-test (MOE_ERR_TIMEOUT is the expected one)."""
+    return int(load().moe_selftest_wait_timeout(int(limit_ms), _stream(stream)))
 
 
 def layer_plan(dims: Dims) -> Plan:
