@@ -38,7 +38,7 @@ METRIC = "MoE layer fwd bf16 TFLOP/s & tokens/s on 1 GB300; % of tensor peak / H
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM0 launch, from a
 # one-pass ncu capture of this benchmark at the configuration's full size; configurations
 # without such a capture report null
-GEMM0_TRAFFIC = {"mixtral": 2014245120 + 457582080}
+GEMM0_TRAFFIC = {"mixtral": 2014122496 + 457581312}
 L2_FLUSH_BYTES = 256 << 20
 
 
