@@ -231,11 +231,14 @@ unsigned char* bytes(void* p) { return static_cast<unsigned char*>(p); }
 // With `fused` (the layer path), GEMM1 also finishes the combine: slot is the
 // whole [n_slots, T, H] array, this launch writes slots slot_j0 .. slot_j0+k-1,
 // and the last contribution to each (token, 256-column tile) writes out.
+// GEMM1 + combine: the row holding the last of n_tickets arrivals per
+// (token, N tile) sums n_slots slots from slot 0 (n_tickets 0 = n_slots).
 struct FusedCombine {
     bool on;
     int32_t slot_j0, n_slots;
     int32_t* arrive;
     uint16_t* out;
+    int32_t n_tickets = 0;
 };
 
 moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, int32_t k,
@@ -284,6 +287,7 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
         b.slot = slot;
         b.slot_j0 = fc.on ? fc.slot_j0 : 0;
         b.n_slots = fc.n_slots;
+        b.n_tickets = fc.n_tickets ? fc.n_tickets : fc.n_slots;
         b.arrive = fc.arrive;
         b.out = fc.out;
         b.ready = ready;
@@ -305,6 +309,7 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
     a.slot = slot;
     a.slot_j0 = fc.on ? fc.slot_j0 : 0;
     a.n_slots = fc.n_slots;
+    a.n_tickets = fc.n_tickets ? fc.n_tickets : fc.n_slots;
     a.arrive = fc.arrive;
     a.out = fc.out;
     MOE_TRY(launch_grouped_gemm(fc.on ? kGemm1Combine : kGemm1Scatter, mh, m2, m2, a, sms, s));
@@ -554,7 +559,9 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     int32_t* arrive = reinterpret_cast<int32_t*>(w + L.arrive);
     const moe_plan plan = plan_of(d);
     const bool fused = plan.combine == MOE_COMBINE_FUSED;
-    if (fused)   // GEMM1 counts contributions per (token, 256-column tile)
+    // GEMM1 counts contributions per (token, 256-column tile); with a shared
+    // expert its GEMM1 runs last and is the only arrival (no counting)
+    if (fused && d.F_shared == 0)
         MOE_TRY(cudaMemsetAsync(arrive, 0, (size_t)d.T * ((d.H + 255) / 256) * 4, s));
 
     record(events ? events->before_route : nullptr, s);
@@ -583,7 +590,8 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                                     tile, offsets, W1, W3, W2, tw, slot,
                                     reinterpret_cast<uint16_t*>(w + L.h), err, sms, s,
                                     events ? events->before_gemm1 : nullptr,
-                                    FusedCombine{fused, 0, n_slots, arrive, out}, cp_gather,
+                                    // with a shared expert, only its GEMM1 (the last) combines
+                                    FusedCombine{fused && d.F_shared == 0, 0, n_slots, arrive, out}, cp_gather,
                                     fuse_gemms ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr));
 
     record(events ? events->before_shared : nullptr, s);
@@ -600,7 +608,8 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                                         nullptr, nullptr, nullptr, W1s, W3s, W2s, sgate,
                                         fused ? slot : slot + (size_t)d.k * d.T * d.H,
                                         reinterpret_cast<uint16_t*>(w + L.hs), err, sms, s, nullptr,
-                                        FusedCombine{fused, d.k, n_slots, arrive, out}));
+                                        // every routed slot is written: one arrival each
+                                        FusedCombine{fused, d.k, n_slots, arrive, out, 1}));
     }
 
     record(events ? events->before_combine : nullptr, s);

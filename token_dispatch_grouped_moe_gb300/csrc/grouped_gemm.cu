@@ -502,6 +502,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // (token, N tile); the holder of the last ticket finishes it
                 const int N1 = FUSED ? args1.N : args.N;
                 const int n_slots = FUSED ? args1.n_slots : args.n_slots;
+                const int n_tickets = FUSED ? args1.n_tickets : args.n_tickets;
                 float* slot = FUSED ? args1.slot : args.slot;
                 uint16_t* out = FUSED ? args1.out : args.out;
                 int32_t* arrive = FUSED ? args1.arrive : args.arrive;
@@ -511,8 +512,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const int f = args.src_row ? args.src_row[p] : p;
                     if (f >= 0 && f / args.k < args.T) {
                         t = f / args.k;
-                        __threadfence();
-                        last = atomicAdd(arrive + t * n_tiles + wk.n_tile, 1) == n_slots - 1;
+                        if (n_tickets == 1) {
+                            last = true;   // the only arrival: every other slot was written before
+                        } else {
+                            __threadfence();
+                            last = atomicAdd(arrive + t * n_tiles + wk.n_tile, 1) == n_tickets - 1;
+                        }
                     }
                 }
                 // the warp sums its finished rows together: lane l takes columns

@@ -97,6 +97,8 @@ struct GemmArgs {
     float* slot;                 // GEMM1: slot array [n_slots, T, N]; rank j goes to slot_j0 + j
     int32_t slot_j0;             // GEMM1: first slot of this launch (the shared expert: k)
     int32_t n_slots;             // kGemm1Combine: contributions summed per (token, N tile)
+    int32_t n_tickets;           // kGemm1Combine: arrivals per (token, N tile) before the sum
+                                 // (n_slots, or 1 when the other slots were written earlier)
     int32_t* arrive;             // kGemm1Combine: [T, ceil(N/256)] tickets, zero before the first launch
     uint16_t* out;               // kGemm1Combine: [T, N] bf16 layer output
     int32_t* ready;              // fused, GEMM1 args: [M tiles] count of GEMM0 warps done, zero first
