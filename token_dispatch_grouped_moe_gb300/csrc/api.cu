@@ -487,11 +487,14 @@ moe_status moe_expert_ffn(const moe_dims* dims, const moe_bf16* x, const int32_t
             x_rows = xp;
         }
     }
+    // the layer's table decides whether both GEMMs share one launch (dense A)
+    const bool fuse_gemms = x_rows && plan_of(*dims).gemm_fusion == MOE_GEMM_FUSION_ON;
     MOE_TRY_STATUS(run_expert_gemms(*dims, R, dims->F, dims->E, dims->k, x, x_rows, src_row, tile,
                                     offsets, W1, W3, W2, topk_w, slot,
                                     reinterpret_cast<uint16_t*>(bytes(ws) + L.h), err, sms, s,
                                     nullptr, FusedCombine{false, 0, 0, nullptr, nullptr},
-                                    a_opt == MOE_GEMM0_A_CP_GATHER));
+                                    a_opt == MOE_GEMM0_A_CP_GATHER,
+                                    fuse_gemms ? reinterpret_cast<int32_t*>(bytes(ws) + L.ready) : nullptr));
     return finish(cudaSuccess, ws, s);
 }
 

@@ -6,7 +6,7 @@
 // p = offsets[e] .. offsets[e+1]-1 hold, in increasing f, the assignments
 // f = t*k + j routed to expert e. Only integer work: the result is bit-exact.
 //
-// Two kernels over fixed chunks of f (kChunk assignments per block):
+// Two phases over fixed chunks of f (kChunk assignments per block):
 //   1. histogram: per-chunk expert counts -> hist[chunk][e];
 //   2. scatter: each block reads the whole (small) hist table to get the
 //      global counts, the exclusive scan over experts and the count of each
@@ -14,7 +14,10 @@
 //      (warp match + per-warp counts in warp order) and writes src_row and
 //      inv_pos. Block 0 also writes counts, offsets and the tile table.
 // No float arithmetic and no order-dependent atomics: the integer atomics in
-// the histogram only count.
+// the histogram only count. While every chunk's block fits on the GPU at once
+// both phases run in one cooperative launch with a grid barrier between them
+// (one launch fewer on the path); larger inputs take two launches.
+#include <cooperative_groups.h>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -30,7 +33,8 @@ constexpr int kScatterThreads = 1024;
 constexpr int kScatterWarps = kScatterThreads / 32;
 constexpr int kMaxE = 256;
 
-__global__ void __launch_bounds__(kHistThreads) perm_hist_kernel(PermuteArgs a)
+// Phase 1 for this block's chunk (any block size).
+__device__ __forceinline__ void hist_body(const PermuteArgs& a)
 {
     __shared__ int hist_s[kMaxE];
     for (int e = threadIdx.x; e < a.E; e += blockDim.x) hist_s[e] = 0;
@@ -48,6 +52,8 @@ __global__ void __launch_bounds__(kHistThreads) perm_hist_kernel(PermuteArgs a)
     for (int e = threadIdx.x; e < a.E; e += blockDim.x)
         a.hist[(int64_t)blockIdx.x * a.E + e] = hist_s[e];
 }
+
+__global__ void __launch_bounds__(kHistThreads) perm_hist_kernel(PermuteArgs a) { hist_body(a); }
 
 // Exclusive scan of vals[0..n) in place by warp 0 (n <= 256); returns total.
 __device__ int warp0_exclusive_scan(int* vals, int n)
@@ -81,7 +87,8 @@ __device__ int warp0_exclusive_scan(int* vals, int n)
     return total;
 }
 
-__global__ void __launch_bounds__(kScatterThreads) perm_scatter_kernel(PermuteArgs a, int n_chunks)
+// Phase 2 for this block's chunk (kScatterThreads threads).
+__device__ __forceinline__ void scatter_body(const PermuteArgs& a, int n_chunks)
 {
     __shared__ int total_s[kMaxE];
     __shared__ int base_s[kMaxE];      // next free position of each expert for this block
@@ -174,6 +181,21 @@ __global__ void __launch_bounds__(kScatterThreads) perm_scatter_kernel(PermuteAr
     }
 }
 
+__global__ void __launch_bounds__(kScatterThreads) perm_scatter_kernel(PermuteArgs a, int n_chunks)
+{
+    scatter_body(a, n_chunks);
+}
+
+// Both phases; launched cooperatively (all blocks resident) so the grid
+// barrier between them completes.
+__global__ void __launch_bounds__(kScatterThreads) perm_fused_kernel(PermuteArgs a, int n_chunks)
+{
+    hist_body(a);
+    __threadfence();
+    cooperative_groups::this_grid().sync();
+    scatter_body(a, n_chunks);
+}
+
 // x_perm[p] = x[src_row[p] / k] for p < offsets[E] (the valid positions;
 // fewer than R only if some expert ids were out of range). src_row null means
 // the identity (f = p); r_valid null means all R rows. One warp per row,
@@ -221,6 +243,19 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s)
         // no assignments: zero counts/offsets/tile table via one tiny block
         perm_scatter_kernel<<<1, kScatterThreads, 0, s>>>(a, 0);
         return cudaGetLastError();
+    }
+    // one cooperative launch while every chunk's block can be resident at once
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, perm_fused_kernel, kScatterThreads, 0) ==
+            cudaSuccess &&
+        n <= sms * per_sm) {
+        PermuteArgs args = a;
+        int n_chunks = n;
+        void* params[] = {&args, &n_chunks};
+        return cudaLaunchCooperativeKernel((const void*)perm_fused_kernel, dim3(n), dim3(kScatterThreads),
+                                           params, 0, s);
     }
     perm_hist_kernel<<<n, kHistThreads, 0, s>>>(a);
     cudaError_t err = cudaGetLastError();
