@@ -36,9 +36,9 @@ from token_dispatch_grouped_moe_gb300.configs import CONFIGS  # noqa: E402
 
 METRIC = "MoE layer fwd bf16 TFLOP/s & tokens/s on 1 GB300; % of tensor peak / HBM BW"
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM0 launch, from a
-# one-pass ncu capture of this benchmark at the configuration's full size; configurations
-# without such a capture report null
-GEMM0_TRAFFIC = {"mixtral": 2014122496 + 457581312}
+# one-pass ncu capture of this benchmark at the configuration's full size, keyed by
+# (configuration, CTAs per MMA); kernels without such a capture report null
+GEMM0_TRAFFIC = {("mixtral", 1): 2014122496 + 457581312, ("mixtral", 2): 2467793920 + 462183168}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -197,9 +197,12 @@ def bench_ours(args, cfg):
                      "separate": lib.COMBINE_SEPARATE}[args.combine])
     lib.set_gemm_fusion({"auto": lib.GEMM_FUSION_AUTO, "on": lib.GEMM_FUSION_ON,
                          "off": lib.GEMM_FUSION_OFF}[args.gemm_fusion])
+    lib.set_cta_group({"auto": lib.CTA_GROUP_AUTO, "one": lib.CTA_GROUP_ONE,
+                       "pair": lib.CTA_GROUP_PAIR}[args.cta_group])
 
     inp, g = make_workload(cfg, device)
     dims = lib.make_dims(cfg.T, cfg.H, cfg.F, cfg.E, cfg.k, cfg.Fs)
+    plan = lib.layer_plan(dims)
     ws = lib.workspace(dims, device=device)
     out = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
@@ -282,7 +285,7 @@ def bench_ours(args, cfg):
     flops = cfg.flops()
     # the library runs both routed GEMMs as one launch below 512 rows per expert
     # (or when forced): then the gemm0 stage holds both and gemm1 is empty
-    fused_gemms = args.gemm_fusion == "on" or (args.gemm_fusion == "auto" and cfg.R < 512 * cfg.E)
+    fused_gemms = plan.gemm_fusion == lib.GEMM_FUSION_ON
     gemm0_ms = float(np.mean(stage_ms["gemm0"]))
     gemm0_flops = 4 * cfg.R * cfg.H * cfg.F + (2 * cfg.R * cfg.F * cfg.H if fused_gemms else 0)
     achieved = gemm0_flops / (gemm0_ms * 1e-3) / 1e12
@@ -311,7 +314,7 @@ def bench_ours(args, cfg):
     value = world * flops / (ms * 1e-3) / 1e12
     # route (+ the top-k pass of the sliced router, E > 8); histogram, scatter,
     # x_perm gather; GEMM0, GEMM1; shared GEMMs; a separate combine unless fused
-    fused = args.combine == "fused" or (args.combine == "auto" and (cfg.Fs or cfg.F) >= 4096)
+    fused = plan.combine == lib.COMBINE_FUSED
     route_launches = 2 if (cfg.E > 8 and cfg.E % 8 == 0) else 1
     launches_per_step = (route_launches + 3 + (1 if fused_gemms else 2) + (2 if cfg.Fs else 0)
                          + (0 if fused else 1))
@@ -336,12 +339,16 @@ def bench_ours(args, cfg):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor",
                      "kernel": "grouped GEMM0 + SwiGLU and GEMM1, one launch (tcgen05)" if fused_gemms
-                     else "grouped GEMM0 + SwiGLU (tcgen05)",
+                     else "grouped GEMM0 + SwiGLU (tcgen05" + (", CTA pairs)" if plan.cta_group == 2
+                                                              else ")"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": None if fused_gemms else GEMM0_TRAFFIC.get(cfg.name),
+                     "traffic": None if fused_gemms else GEMM0_TRAFFIC.get((cfg.name, plan.cta_group)),
                      "traffic_unit": "bytes per launch",
                      "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"},
+        "gemm_plan": {"cta_group": plan.cta_group, "cta_group_gemm1": plan.cta_group_gemm1,
+                      "tile": [plan.tile_m, plan.tile_n, plan.tile_k],
+                      "stages": plan.stages, "one_launch": fused_gemms, "combine_fused": fused},
         "stage_ms": stage_summary,
         "stage_roofline": stage_roofline,
         "e2e": {"value": round(world * flops / (e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
@@ -422,6 +429,8 @@ def main():
                     help="where the layer sums the expert rows (GEMM1 epilogue or a separate kernel)")
     ap.add_argument("--gemm-fusion", default="auto", choices=["auto", "on", "off"],
                     help="both routed GEMMs in one persistent launch, or two launches")
+    ap.add_argument("--cta-group", default="auto", choices=["auto", "one", "pair"],
+                    help="CTAs per tensor-core MMA in the dense-A expert GEMMs")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--ref-tokens", type=int, default=64, help="oracle tokens per reference step")
     args = ap.parse_args()

@@ -146,7 +146,21 @@ enum {
     MOE_OPT_GEMM_FUSION = 2,
     MOE_GEMM_FUSION_AUTO = 0,
     MOE_GEMM_FUSION_ON = 1,
-    MOE_GEMM_FUSION_OFF = 2
+    MOE_GEMM_FUSION_OFF = 2,
+    /* How many CTAs share one tensor-core MMA in the expert GEMMs that read a
+     * dense A operand (GEMM0 over x_perm, every GEMM1, the shared expert):
+     *   MOE_CTA_GROUP_AUTO (default) the table in the library's layer call
+     *                      (by rows per expert and GEMM; see moe_layer_plan);
+     *   MOE_CTA_GROUP_ONE  one CTA per 128 x 256 MMA tile;
+     *   MOE_CTA_GROUP_PAIR a 2-CTA cluster per 256 x 256 MMA tile
+     *                      (tcgen05 cta_group::2): each CTA stages 128 rows
+     *                      of A and half of B's columns.
+     * The gathered GEMM0 forms and the one-launch GEMM pair always run one CTA
+     * per MMA. */
+    MOE_OPT_CTA_GROUP = 3,
+    MOE_CTA_GROUP_AUTO = 0,
+    MOE_CTA_GROUP_ONE = 1,
+    MOE_CTA_GROUP_PAIR = 2
 };
 
 /* Sets a library-wide option for later calls (all devices and threads).
@@ -173,11 +187,14 @@ typedef struct {
     int32_t gemm0_a;       /* MOE_GEMM0_A_* in effect */
     int32_t combine;       /* MOE_COMBINE_FUSED or MOE_COMBINE_SEPARATE */
     int32_t gemm_fusion;   /* MOE_GEMM_FUSION_ON or MOE_GEMM_FUSION_OFF */
-    int32_t tile_m;        /* grouped GEMM tile rows (routed rows per tile) */
+    int32_t tile_m;        /* grouped GEMM tile rows (routed rows per tile; 256 for a CTA pair) */
     int32_t tile_n;        /* grouped GEMM MMA N (GEMM0: half W1, half W3) */
     int32_t tile_k;        /* K per pipeline stage */
     int32_t stages;        /* shared-memory pipeline stages */
-    int32_t cta_group;     /* CTAs per MMA (tcgen05 cta_group) */
+    int32_t cta_group;     /* CTAs per MMA (tcgen05 cta_group) of the routed GEMM0; tile_m
+                            * and stages describe it */
+    int32_t cta_group_gemm1; /* the same for the routed GEMM1 (a second launch; 1 when both
+                              * GEMMs share one launch) */
 } moe_plan;
 
 /* Fills *plan for `dims` (host only: no device work, no launch). Returns

@@ -94,8 +94,8 @@ def test_options(L):
     assert lib.get_gemm0_a() == lib.GEMM0_A_TMA_GATHER
     lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
     assert L.moe_set_option(0, 7) == 1
-    assert L.moe_set_option(4, 0) == 1
-    assert L.moe_get_option(4) == -1
+    assert L.moe_set_option(5, 0) == 1
+    assert L.moe_get_option(5) == -1
     assert lib.get_combine() == lib.COMBINE_AUTO
     for mode in (lib.COMBINE_FUSED, lib.COMBINE_SEPARATE, lib.COMBINE_AUTO):
         lib.set_combine(mode)
@@ -106,6 +106,11 @@ def test_options(L):
         lib.set_gemm_fusion(mode)
         assert lib.get_gemm_fusion() == mode
     assert L.moe_set_option(2, 3) == 1
+    assert lib.get_cta_group() == lib.CTA_GROUP_AUTO
+    for mode in (lib.CTA_GROUP_ONE, lib.CTA_GROUP_PAIR, lib.CTA_GROUP_AUTO):
+        lib.set_cta_group(mode)
+        assert lib.get_cta_group() == mode
+    assert L.moe_set_option(3, 3) == 1
 
 
 def test_zero_tokens_is_noop_on_host(L):
@@ -117,24 +122,44 @@ def test_zero_tokens_is_noop_on_host(L):
 
 
 def test_layer_plan_table(L):
-    """The per-shape table: router, combine form and GEMM fusion chosen for the
-    layer configurations (host only), and the options that override it."""
+    """The per-shape table: router, combine form, GEMM fusion and CTAs per MMA
+    chosen for the layer configurations (host only), and the options that
+    override it."""
     from token_dispatch_grouped_moe_gb300 import lib
     from token_dispatch_grouped_moe_gb300.configs import CONFIGS
-    want = {   # config: (router, combine, gemm_fusion)
-        "tiny": (lib.ROUTER_STREAM, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON),
-        "mixtral": (lib.ROUTER_STREAM, lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF),
-        "qwen2": (lib.ROUTER_SLICED, lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF),
-        "dsk-1k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON),
-        "dsk-4k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON),
-        "dsk-32k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_OFF),
+    want = {   # config: (router, combine, gemm_fusion, CTAs per MMA of GEMM0 and of GEMM1)
+        "tiny": (lib.ROUTER_STREAM, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON, 1, 1),
+        "mixtral": (lib.ROUTER_STREAM, lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF, 2, 2),
+        "qwen2": (lib.ROUTER_SLICED, lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF, 1, 2),
+        "dsk-1k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON, 1, 1),
+        "dsk-4k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON, 1, 1),
+        "dsk-16k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_OFF, 2, 2),
+        "dsk-32k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_OFF, 2, 2),
     }
-    for name, (router, combine, fusion) in want.items():
+    for name, (router, combine, fusion, cg, cg1) in want.items():
         c = CONFIGS[name]
         p = lib.layer_plan(lib.make_dims(c.T, c.H, c.F, c.E, c.k, c.Fs))
-        assert (p.router, p.combine, p.gemm_fusion) == (router, combine, fusion), name
-        assert (p.gemm0_a, p.tile_m, p.tile_n, p.tile_k, p.stages, p.cta_group) == (
-            lib.GEMM0_A_PERMUTED, 128, 256, 64, 4, 1)
+        assert (p.router, p.combine, p.gemm_fusion, p.cta_group, p.cta_group_gemm1) == (
+            router, combine, fusion, cg, cg1), name
+        tile = (256, 256, 64, 6) if cg == 2 else (128, 256, 64, 4)
+        assert (p.gemm0_a, p.tile_m, p.tile_n, p.tile_k, p.stages) == (lib.GEMM0_A_PERMUTED, *tile), name
+    # the CTA-group option overrides the table; a gather A path runs one CTA
+    d = lib.make_dims(8192, 4096, 14336, 8, 2)
+    try:
+        lib.set_cta_group(lib.CTA_GROUP_ONE)
+        assert (lib.layer_plan(d).cta_group, lib.layer_plan(d).cta_group_gemm1) == (1, 1)
+        lib.set_cta_group(lib.CTA_GROUP_PAIR)
+        small = lib.make_dims(64, 256, 64, 8, 2)
+        assert (lib.layer_plan(small).cta_group, lib.layer_plan(small).cta_group_gemm1) == (1, 1)  # one launch
+        lib.set_gemm_fusion(lib.GEMM_FUSION_OFF)
+        assert (lib.layer_plan(small).cta_group, lib.layer_plan(small).cta_group_gemm1) == (2, 2)
+        lib.set_cta_group(lib.CTA_GROUP_AUTO)
+        lib.set_gemm0_a(lib.GEMM0_A_TMA_GATHER)
+        assert (lib.layer_plan(d).cta_group, lib.layer_plan(d).cta_group_gemm1) == (1, 2)
+    finally:
+        lib.set_cta_group(lib.CTA_GROUP_AUTO)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
+        lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
     # E not a multiple of 8, E > 64, a gate too large for the streaming router
     assert lib.layer_plan(lib.make_dims(64, 256, 64, 12, 2)).router == lib.ROUTER_CLUSTER
     assert lib.layer_plan(lib.make_dims(64, 256, 64, 200, 2)).router == lib.ROUTER_SLICED

@@ -392,6 +392,59 @@ def test_gemm_fusion_bit_identical(lib, shape):
         assert torch.equal(outs[0], o)
 
 
+# shapes for the CTA-pair GEMMs: experts whose last 256-row tile leaves the
+# second CTA no rows, the last tile running past the dispatched rows, a GEMM0 N
+# tail (F % 128 == 64), a GEMM1 N tail in the second CTA's half (H % 256 ==
+# 192), 256 groups (the in-kernel tile-table scan), a single group (the shared
+# expert), and every shape well below and above one 256-row tile per expert
+PAIR_SHAPES = [(300, 256, 192, 8, 2, 0), (257, 192, 128, 64, 6, 0), (200, 256, 128, 16, 4, 384),
+               (64, 128, 64, 256, 8, 0), (1500, 512, 1408, 8, 2, 0), (3, 64, 64, 3, 2, 0),
+               (77, 256, 320, 5, 3, 0), (2100, 448, 320, 4, 2, 640)]
+
+
+@pytest.mark.parametrize("shape", PAIR_SHAPES)
+def test_cta_pair_bit_identical(lib, shape):
+    """A 2-CTA cluster per 256-row MMA tile (tcgen05 cta_group::2) gives the
+    same bits as one CTA per 128-row tile, with either combine form."""
+    T, H, F, E, k, Fs = shape
+    inp = make_inputs(T, H, F, E, Fs=Fs, seed=17)
+    g = {n: v.cuda() for n, v in inp.items()}
+    dims = lib.make_dims(T, H, F, E, k, Fs)
+    ws = lib.workspace(dims)
+    outs = []
+    try:
+        lib.set_gemm_fusion(lib.GEMM_FUSION_OFF)
+        for combine in (lib.COMBINE_SEPARATE, lib.COMBINE_FUSED):
+            lib.set_combine(combine)
+            for cg in (lib.CTA_GROUP_ONE, lib.CTA_GROUP_PAIR, lib.CTA_GROUP_PAIR):
+                lib.set_cta_group(cg)
+                outs.append(lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws,
+                                              W1s=g.get("W1s"), W3s=g.get("W3s"),
+                                              W2s=g.get("W2s")).clone())
+    finally:
+        lib.set_cta_group(lib.CTA_GROUP_AUTO)
+        lib.set_combine(lib.COMBINE_AUTO)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "f_tail", "h_tail_e64", "dense_e1", "shared",
+                                  "one_token", "e256"])
+def test_small_case_cta_pair(lib, oracle, name):
+    """Edge cases with the expert GEMMs on CTA pairs, against the oracle."""
+    T, H, F, E, k, Fs = SMALL_CASES[name]
+    lib.set_gemm_fusion(lib.GEMM_FUSION_OFF)
+    lib.set_cta_group(lib.CTA_GROUP_PAIR)
+    try:
+        run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=5, tol="elementwise")
+    finally:
+        lib.set_cta_group(lib.CTA_GROUP_AUTO)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
+
+
 @pytest.mark.parametrize("name", ["tiny", "ragged", "f_tail", "h_tail_e64", "shared", "one_token", "e256"])
 def test_small_case_fused_gemms(lib, oracle, name):
     """Edge cases with both routed GEMMs in one launch, against the oracle."""
@@ -447,9 +500,21 @@ def test_deterministic(lib, oracle):
     assert torch.equal(o1, o2)
 
 
-def test_stage_api_matches_layer(lib, oracle):
+@pytest.mark.parametrize("gemms", ["auto", "cta_pair"])
+def test_stage_api_matches_layer(lib, oracle, gemms):
     """route -> permute -> expert_ffn -> combine equals moe_layer_forward bit for bit;
     x_perm equals x gathered by src_row."""
+    if gemms == "cta_pair":
+        lib.set_gemm_fusion(lib.GEMM_FUSION_OFF)
+        lib.set_cta_group(lib.CTA_GROUP_PAIR)
+    try:
+        _stage_api_matches_layer(lib)
+    finally:
+        lib.set_cta_group(lib.CTA_GROUP_AUTO)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
+
+
+def _stage_api_matches_layer(lib):
     T, H, F, E, k, Fs = 300, 256, 192, 8, 2, 128
     inp = make_inputs(T, H, F, E, Fs=Fs, seed=7)
     g = {n: v.cuda() for n, v in inp.items()}

@@ -25,6 +25,7 @@ std::atomic<int> g_num_sms[kMaxDevices];
 std::atomic<int> g_gemm0_a{MOE_GEMM0_A_PERMUTED};
 std::atomic<int> g_combine{MOE_COMBINE_AUTO};
 std::atomic<int> g_gemm_fusion{MOE_GEMM_FUSION_AUTO};
+std::atomic<int> g_cta_group{MOE_CTA_GROUP_AUTO};
 
 int num_sms_current()
 {
@@ -116,9 +117,29 @@ bool make_map_b(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer
 //    (DeepSeek-shaped T = 1024: 0.273 -> 0.259 ms per layer, T = 4096:
 //    0.484 -> 0.467 ms); from 512 rows per expert up (Qwen2, DeepSeek
 //    T = 32768, Mixtral) the two forms measured the same;
-//  - one compiled GEMM tile: 128 x 256 x 64, 4 stages, one CTA per MMA. Zipf
-//    routing needs no reordering: the static schedule spreads every expert's
-//    tiles over all SMs (Mixtral-Zipf measured as fast as uniform routing).
+//  - CTAs per MMA (dense-A GEMMs, not in the one-launch pair): a 2-CTA
+//    cluster per 256 x 256 x 64 tile (tcgen05 cta_group::2, 6 stages of 32 KB
+//    in each CTA) for GEMM0 from 1024 dispatched rows per expert on average
+//    and for GEMM1 from 512; else one CTA per 128 x 256 x 64 tile (4 stages of
+//    48 KB). Measured per layer, one CTA -> pairs: DeepSeek T = 32768 2.87 ->
+//    2.76 ms (GEMM1 0.80 -> 0.72), T = 16384 1.49 -> 1.43, Qwen2 2.55 -> 2.49
+//    (GEMM0 0.85 -> 0.87: 512 rows per expert pad more in 256-row tiles),
+//    Mixtral 3.53 -> 3.51. Zipf routing needs no reordering: the static
+//    schedule spreads every expert's tiles over all SMs (Mixtral-Zipf measured
+//    as fast as uniform routing).
+// CTAs per MMA for an expert GEMM over `rows` dispatched rows in `groups`
+// experts (option, else the table): a pair's 256-row tiles pad each expert to
+// a multiple of 256 rows, which costs GEMM0 more than the pair gains below
+// 1024 rows per expert; GEMM1 gains more (its short K leaves a 4-stage ring
+// of 48 KB exposed at every tile) and takes pairs from 512.
+int cta_group_for(int64_t rows, int32_t groups, bool gemm1)
+{
+    const int opt = g_cta_group.load();
+    if (opt == MOE_CTA_GROUP_ONE) return 1;
+    if (opt == MOE_CTA_GROUP_PAIR) return 2;
+    return rows >= (int64_t)(gemm1 ? 512 : 1024) * groups ? 2 : 1;
+}
+
 moe_plan plan_of(const moe_dims& d)
 {
     moe_plan p{};
@@ -133,11 +154,13 @@ moe_plan plan_of(const moe_dims& d)
                       (fusion_opt == MOE_GEMM_FUSION_ON ||
                        (fusion_opt == MOE_GEMM_FUSION_AUTO && d.T * (int64_t)d.k < (int64_t)512 * d.E));
     p.gemm_fusion = fuse ? MOE_GEMM_FUSION_ON : MOE_GEMM_FUSION_OFF;
-    p.tile_m = kTileM;
+    p.cta_group = (p.gemm0_a == MOE_GEMM0_A_PERMUTED && !fuse)
+                      ? cta_group_for(d.T * (int64_t)d.k, d.E, false) : 1;
+    p.cta_group_gemm1 = fuse ? 1 : cta_group_for(d.T * (int64_t)d.k, d.E, true);
+    p.tile_m = p.cta_group == 2 ? 2 * kTileM : kTileM;
     p.tile_n = 256;
     p.tile_k = 64;
-    p.stages = 4;
-    p.cta_group = 1;
+    p.stages = p.cta_group == 2 ? 6 : 4;
     return p;
 }
 
@@ -247,7 +270,8 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
                             const uint16_t* W3, const uint16_t* W2, const float* topk_w, float* slot,
                             uint16_t* h, uint32_t* err, int sms, cudaStream_t s, moe_event_t ev_mid,
                             const FusedCombine& fc = FusedCombine{false, 0, 0, nullptr, nullptr},
-                            bool cp_gather = false, int32_t* ready = nullptr)
+                            bool cp_gather = false, int32_t* ready = nullptr, int cta_group0 = 1,
+                            int cta_group1 = 1)
 {
     if (M == 0) {
         if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
@@ -299,7 +323,7 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
         return MOE_OK;
     }
     MOE_TRY(launch_grouped_gemm(dense ? kGemm0Dense : cp_gather ? kGemm0CpGather : kGemm0Gather, mx, m1,
-                                m3, a, sms, s));
+                                m3, a, sms, s, dense ? cta_group0 : 1));
     if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
     // GEMM1 + weighted scatter: h [rows, F] x W2 [F, H] -> slot[rank][token]
     a.N = d.H;
@@ -312,7 +336,7 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
     a.n_tickets = fc.n_tickets ? fc.n_tickets : fc.n_slots;
     a.arrive = fc.arrive;
     a.out = fc.out;
-    MOE_TRY(launch_grouped_gemm(fc.on ? kGemm1Combine : kGemm1Scatter, mh, m2, m2, a, sms, s));
+    MOE_TRY(launch_grouped_gemm(fc.on ? kGemm1Combine : kGemm1Scatter, mh, m2, m2, a, sms, s, cta_group1));
     return MOE_OK;
 }
 
@@ -365,6 +389,12 @@ moe_status moe_set_option(int option, int value)
         g_gemm_fusion.store(value);
         return MOE_OK;
     }
+    if (option == MOE_OPT_CTA_GROUP) {
+        if (value != MOE_CTA_GROUP_AUTO && value != MOE_CTA_GROUP_ONE && value != MOE_CTA_GROUP_PAIR)
+            return MOE_ERR_INVALID_ARG;
+        g_cta_group.store(value);
+        return MOE_OK;
+    }
     return MOE_ERR_INVALID_ARG;
 }
 
@@ -373,6 +403,7 @@ int moe_get_option(int option)
     if (option == MOE_OPT_GEMM0_A) return g_gemm0_a.load();
     if (option == MOE_OPT_COMBINE) return g_combine.load();
     if (option == MOE_OPT_GEMM_FUSION) return g_gemm_fusion.load();
+    if (option == MOE_OPT_CTA_GROUP) return g_cta_group.load();
     return -1;
 }
 
@@ -488,13 +519,15 @@ moe_status moe_expert_ffn(const moe_dims* dims, const moe_bf16* x, const int32_t
         }
     }
     // the layer's table decides whether both GEMMs share one launch (dense A)
-    const bool fuse_gemms = x_rows && plan_of(*dims).gemm_fusion == MOE_GEMM_FUSION_ON;
+    const moe_plan plan = plan_of(*dims);
+    const bool fuse_gemms = x_rows && plan.gemm_fusion == MOE_GEMM_FUSION_ON;
     MOE_TRY_STATUS(run_expert_gemms(*dims, R, dims->F, dims->E, dims->k, x, x_rows, src_row, tile,
                                     offsets, W1, W3, W2, topk_w, slot,
                                     reinterpret_cast<uint16_t*>(bytes(ws) + L.h), err, sms, s,
                                     nullptr, FusedCombine{false, 0, 0, nullptr, nullptr},
                                     a_opt == MOE_GEMM0_A_CP_GATHER,
-                                    fuse_gemms ? reinterpret_cast<int32_t*>(bytes(ws) + L.ready) : nullptr));
+                                    fuse_gemms ? reinterpret_cast<int32_t*>(bytes(ws) + L.ready) : nullptr,
+                                    plan.cta_group, plan.cta_group_gemm1));
     return finish(cudaSuccess, ws, s);
 }
 
@@ -595,7 +628,8 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                                     events ? events->before_gemm1 : nullptr,
                                     // with a shared expert, only its GEMM1 (the last) combines
                                     FusedCombine{fused && d.F_shared == 0, 0, n_slots, arrive, out}, cp_gather,
-                                    fuse_gemms ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr));
+                                    fuse_gemms ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr,
+                                    plan.cta_group, plan.cta_group_gemm1));
 
     record(events ? events->before_shared : nullptr, s);
     if (d.F_shared > 0) {
@@ -612,7 +646,9 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                                         fused ? slot : slot + (size_t)d.k * d.T * d.H,
                                         reinterpret_cast<uint16_t*>(w + L.hs), err, sms, s, nullptr,
                                         // every routed slot is written: one arrival each
-                                        FusedCombine{fused, d.k, n_slots, arrive, out, 1}));
+                                        FusedCombine{fused, d.k, n_slots, arrive, out, 1}, false, nullptr,
+                                        (permuted || cp_gather) ? cta_group_for(d.T, 1, false) : 1,
+                                        cta_group_for(d.T, 1, true)));
     }
 
     record(events ? events->before_combine : nullptr, s);

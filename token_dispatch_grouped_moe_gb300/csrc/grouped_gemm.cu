@@ -50,6 +50,7 @@
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time.
 // Every wait is bounded (ptx.cuh); on a timeout the CTA drains what it
 // issued, frees its TMEM and exits with the error recorded.
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -65,18 +66,29 @@ constexpr int BM = kTileM;   // 128
 constexpr int BN = 256;      // MMA N (GEMM0: 128 of W1 + 128 of W3)
 constexpr int BK = kGemmBK;  // K per stage: one A row of BK bf16 = one swizzle span
 constexpr int A_ROW = BK * 2;                // bytes: 64 (64-byte swizzle) or 128 (128-byte)
-constexpr int STAGES = BK == 32 ? 9 : 4;     // 9 x 24 KB or 4 x 48 KB of shared memory
 static_assert(BK == 32 || BK == 64, "A rows are one 64- or 128-byte swizzle span");
 constexpr int A_BYTES = BM * BK * 2;         // 8 KB (BK 32) or 16 KB
-constexpr int B_BYTES = BN * BK * 2;         // 16 KB (BK 32) or 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int B_CHUNK_BYTES = BK * 128;      // one 64-column slice of B: BK k-rows x 128 B
 constexpr int NUM_THREADS = 224;   // 7 warps: TMA, MMA, 4 x epilogue, row gather
 constexpr int GATHER_LAG = 2;      // stages a gathered A tile is given to land
 constexpr int MAX_GROUPS = 257;
 constexpr int TMEM_COLS = 512;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
 
+// One CTA per MMA (PAIR false): a stage holds A 128 x BK and all BN columns of
+// B. A CTA pair (PAIR true, tcgen05 cta_group::2): one MMA of 256 x BN over
+// both CTAs, each staging its 128 rows of A and its BN / 2 columns of B, so a
+// stage is 32 KB instead of 48 KB and 6 stages fit where 4 did.
+template <bool PAIR>
+struct Cfg {
+    static constexpr int B_COLS = PAIR ? BN / 2 : BN;   // columns of B staged by this CTA
+    static constexpr int B_BYTES = B_COLS * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = PAIR ? 6 : (BK == 32 ? 9 : 4);
+    static constexpr int TILE_ROWS = PAIR ? 2 * BM : BM;   // rows of one work item
+    static constexpr uint32_t IDESC = idesc_bf16_f32(TILE_ROWS, BN, /*a_mn_major=*/false, /*b_mn_major=*/true);
+};
+
+template <int STAGES>
 struct SmemTail {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -90,14 +102,23 @@ struct SmemTail {
     int tok[BM];                      // kGemm0CpGather: token of each row of the current tile
 };
 
-constexpr size_t SMEM_BYTES = 1024 /*align slack*/ + (size_t)STAGES * STAGE_BYTES + sizeof(SmemTail);
+template <bool PAIR>
+constexpr size_t smem_bytes()
+{
+    return 1024 /*align slack*/ + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES +
+           sizeof(SmemTail<Cfg<PAIR>::STAGES>);
+}
+static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory");
 
 struct Work {
     int g, row0, rows, n_tile;
 };
 
 // Work item w of the static schedule: expert-major, then N tile, then M tile.
-__device__ __forceinline__ Work decode_work(int w, int n_tiles, const int* ts, const int* offs, int G)
+// ts is the table of TILE_ROWS-row tiles; this CTA's rows start `sub` rows into
+// the tile (a pair's rank-1 CTA: 128) and may be none (rows <= 0).
+template <int TILE_ROWS>
+__device__ __forceinline__ Work decode_work(int w, int n_tiles, const int* ts, const int* offs, int G, int sub)
 {
     int lo = 0, hi = G;   // ts[lo]*n <= w < ts[hi]*n
     while (hi - lo > 1) {
@@ -110,12 +131,12 @@ __device__ __forceinline__ Work decode_work(int w, int n_tiles, const int* ts, c
     const int wl = w - ts[lo] * n_tiles;
     r.n_tile = wl / mt;
     const int ml = wl - r.n_tile * mt;
-    r.row0 = offs[lo] + ml * BM;
+    r.row0 = offs[lo] + ml * TILE_ROWS + sub;
     r.rows = min(BM, offs[lo + 1] - r.row0);
     return r;
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmA1,
@@ -125,7 +146,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t tiles_addr = (raw_addr + 1023u) & ~1023u;
     unsigned char* tiles = smem_raw + (tiles_addr - raw_addr);
-    SmemTail* st = reinterpret_cast<SmemTail*>(tiles + (size_t)STAGES * STAGE_BYTES);
+    using C = Cfg<PAIR>;
+    constexpr int STAGES = C::STAGES;
+    constexpr int STAGE_BYTES = C::STAGE_BYTES;
+    constexpr int CG = PAIR ? 2 : 1;   // tcgen05 CTA group
+    SmemTail<STAGES>* st = reinterpret_cast<SmemTail<STAGES>*>(tiles + (size_t)STAGES * STAGE_BYTES);
 
     // FUSED: work items [0, total0) are GEMM0 (dense A) tiles, the rest GEMM1
     // tiles (args1, maps tmA1 / tmB2); a GEMM1 tile waits until every GEMM0
@@ -136,9 +161,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr bool COMBINE = (MODE == kGemm1Combine || MODE == kFusedCombine);
     constexpr bool CP_GATHER = (MODE == kGemm0CpGather);
     constexpr bool GATHER = (MODE == kGemm0Gather);
+    static_assert(!PAIR || MODE == kGemm0Dense || MODE == kGemm1Scatter || MODE == kGemm1Combine,
+                  "CTA pairs run the dense-A GEMM0 and the GEMM1 modes");
+    static_assert(!PAIR || BK == 64, "CTA pairs use 128-byte rows of A");
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int G = args.G;
+    // a pair walks the schedule together: both CTAs take the same work items,
+    // rank 0 the first 128 rows of each and rank 1 the next 128
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+    const int unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+    const int n_units = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int sub = (int)rank * BM;
 
     // ---- set-up
     if (threadIdx.x == 0) {
@@ -150,13 +184,49 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(smem_u32(&st->tfull[a]), 1);
-            mbar_init(smem_u32(&st->tempty[a]), 4);
+            // the epilogue warps release a TMEM buffer: 4 here, 4 more from the peer
+            mbar_init(smem_u32(&st->tempty[a]), PAIR ? 8 : 4);
         }
         mbar_init(smem_u32(&st->drain), 1);
         st->abort = 0;
         fence_barrier_init();
     }
-    if (args.tile_start == nullptr) {
+    if (PAIR) {
+        // the table of 256-row tiles, from the group offsets (warp 0: a scan)
+        if (warp == 0) {
+            if (args.tile_start == nullptr) {
+                if (lane == 0) {
+                    st->offsets[0] = 0;
+                    st->offsets[1] = args.M;
+                }
+            } else {
+                for (int i = lane; i <= G; i += 32) st->offsets[i] = args.offsets[i];
+            }
+            __syncwarp();
+            const int per = (G + 31) / 32;
+            const int g0 = lane * per;
+            auto tiles_of = [&](int g) {
+                return (st->offsets[g + 1] - st->offsets[g] + C::TILE_ROWS - 1) / C::TILE_ROWS;
+            };
+            int mine = 0;
+            for (int i = 0; i < per; ++i)
+                if (g0 + i < G) mine += tiles_of(g0 + i);
+            int incl = mine;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += v;
+            }
+            int run = incl - mine;
+            for (int i = 0; i < per; ++i) {
+                if (g0 + i < G) {
+                    st->tile_start[g0 + i] = run;
+                    run += tiles_of(g0 + i);
+                }
+            }
+            if (lane == 31) st->tile_start[G] = incl;
+        }
+    } else if (args.tile_start == nullptr) {
         if (threadIdx.x == 0) {
             st->tile_start[0] = 0;
             st->tile_start[1] = (args.M + BM - 1) / BM;
@@ -179,11 +249,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(&st->tmem_base), TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<CG>(smem_u32(&st->tmem_base), TMEM_COLS);
+        tmem_relinquish<CG>();
     }
     tc_fence_before();
-    __syncthreads();
+    // a pair: both CTAs' barriers are initialised before either signals the other's
+    if (PAIR) cluster_sync(); else __syncthreads();
     tc_fence_after();
 
     const uint32_t tmem_base = st->tmem_base;
@@ -203,11 +274,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t phase = 0;
         int issued = 0;
         bool ok = true;
-        for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+        for (int w = unit; w < total && ok; w += n_units) {
             const bool p1 = FUSED && w >= total0;
             const int n_tiles = p1 ? n_tiles1 : n_tiles0;
             const int k_blocks = p1 ? k_blocks1 : k_blocks0;
-            const Work wk = decode_work(p1 ? w - total0 : w, n_tiles, st->tile_start, st->offsets, G);
+            const Work wk = decode_work<C::TILE_ROWS>(p1 ? w - total0 : w, n_tiles, st->tile_start, st->offsets,
+                                                     G, sub);
             if (p1) {
                 // the rows of h this tile reads: every GEMM0 tile of (expert, M tile)
                 // must have stored and published them
@@ -246,7 +318,31 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint32_t full = smem_u32(&st->full[stage]);
                 const uint32_t a_dst = tiles_addr + stage * STAGE_BYTES;
                 const uint32_t b_dst = a_dst + A_BYTES;
-                if (lane == 0) mbar_arrive_expect_tx(full, CP_GATHER ? B_BYTES : STAGE_BYTES);
+                if constexpr (PAIR) {
+                    // both CTAs' boxes complete on the leader's barrier, which
+                    // expects the bytes of the two
+                    if (lane == 0) {
+                        if (rank == 0) mbar_arrive_expect_tx(full, 2 * STAGE_BYTES);
+                        const uint32_t bar = mapa_shared(full, 0);
+                        tma_load_2d_pair(a_dst, &tmA, kb * BK, wk.row0, bar);
+                        if (HAS_GEMM0) {
+                            // rank 0 stages the W1 half of B, rank 1 the W3 half
+                            const CUtensorMap* mb = rank == 0 ? &tmB0 : &tmB1;
+                            const int n0 = wk.n_tile * (BN / 2);
+                            tma_load_2d_pair(b_dst, mb, n0, b_row + kb * BK, bar);
+                            tma_load_2d_pair(b_dst + B_CHUNK_BYTES, mb, n0 + 64, b_row + kb * BK, bar);
+                        } else {
+                            const int n0 = wk.n_tile * BN + (int)rank * (BN / 2);
+                            tma_load_2d_pair(b_dst, &tmB0, n0, b_row + kb * BK, bar);
+                            tma_load_2d_pair(b_dst + B_CHUNK_BYTES, &tmB0, n0 + 64, b_row + kb * BK, bar);
+                        }
+                    }
+                    __syncwarp();
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    continue;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(full, CP_GATHER ? C::B_BYTES : STAGE_BYTES);
                 __syncwarp();
                 if (GATHER)
                     tma_gather4(a_dst + lane * 4 * A_ROW, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], full);
@@ -273,7 +369,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
-        if (!ok && lane == 0) {
+        if (PAIR && ok) {
+            // the tensor-core commits that free this CTA's stages come from the
+            // leader; wait for the last of them to land before the CTA may exit
+            for (int i = 0; i < STAGES; ++i) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait(smem_u32(&st->empty[stage]), phase ^ 1u, abort, args.err)))
+                    break;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!PAIR && !ok && lane == 0) {
             // drain: wait (bounded) for the loads still in flight
             int s = stage;
             uint32_t ph = phase;
@@ -284,16 +390,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     } else if (warp == 1) {
         // ============================ MMA issuer ==============================
-        if (lane == 0) {
+        // (a pair: the rank-0 CTA issues for both)
+        if (lane == 0 && rank == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
             bool any = false;
-            for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
+            for (int w = unit; w < total && ok; w += n_units) {
                 const int k_blocks = (FUSED && w >= total0) ? k_blocks1 : k_blocks0;
-                if (!mbar_wait(smem_u32(&st->tempty[acc]), acc_phase ^ 1u, abort, args.err)) {
+                if (!mbar_wait<PAIR>(smem_u32(&st->tempty[acc]), acc_phase ^ 1u, abort, args.err)) {
                     ok = false;
                     break;
                 }
@@ -313,19 +420,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const uint64_t ad = BK == 64 ? smem_desc_sw128(a_base + kk * 32, 16, 1024)
                                                      : smem_desc_sw64(a_base + kk * 32, 16, 512);
                         const uint64_t bd = smem_desc_sw128(b_base + kk * 16 * 128, B_CHUNK_BYTES, 1024);
-                        tc_mma_f16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        tc_mma_f16<CG>(d_tmem, ad, bd, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
                     }
                     any = true;
-                    tc_commit(smem_u32(&st->empty[stage]));
+                    tc_commit<CG>(smem_u32(&st->empty[stage]));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (!ok) break;
-                tc_commit(smem_u32(&st->tfull[acc]));
+                tc_commit<CG>(smem_u32(&st->tfull[acc]));
                 if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             if (!ok && any) {
                 // drain: every MMA issued so far must finish before TMEM is freed
-                tc_commit(smem_u32(&st->drain));
+                if (PAIR) tc_commit_pair_local(smem_u32(&st->drain));
+                else tc_commit(smem_u32(&st->drain));
                 mbar_wait_drain(smem_u32(&st->drain), 0);
             }
         }
@@ -352,7 +460,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int n_tiles = n_tiles0;
             const int k_blocks = k_blocks0;
             for (int w = blockIdx.x; w < total && ok; w += gridDim.x) {
-                const Work wk = decode_work(w, n_tiles, st->tile_start, st->offsets, G);
+                const Work wk = decode_work<BM>(w, n_tiles, st->tile_start, st->offsets, G, 0);
                 __syncwarp();   // the previous tile's rows are no longer read
                 for (int rr = lane; rr < BM; rr += 32) {
                     const int p = wk.row0 + min(rr, wk.rows - 1);
@@ -403,10 +511,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const int r = ew * 32 + lane;          // row of the tile
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int w = blockIdx.x; w < total; w += gridDim.x) {
+        for (int w = unit; w < total; w += n_units) {
             const bool p1 = FUSED && w >= total0;
             const int n_tiles = p1 ? n_tiles1 : n_tiles0;
-            const Work wk = decode_work(p1 ? w - total0 : w, n_tiles, st->tile_start, st->offsets, G);
+            const Work wk = decode_work<C::TILE_ROWS>(p1 ? w - total0 : w, n_tiles, st->tile_start, st->offsets,
+                                                     G, sub);
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&st->tfull[acc]), acc_phase, abort, args.err)))
                 break;
             tc_fence_after();
@@ -496,7 +605,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&st->tempty[acc]));   // TMEM free for the MMA
+            if (lane == 0) {
+                // TMEM free for the MMA (a pair's: on the leader's barrier)
+                if (PAIR && rank != 0) mbar_arrive_remote(mapa_shared(smem_u32(&st->tempty[acc]), 0));
+                else mbar_arrive(smem_u32(&st->tempty[acc]));
+            }
             if (COMBINE && (!FUSED || p1)) {
                 // publish this row's slot segment, then take a ticket for its
                 // (token, N tile); the holder of the last ticket finishes it
@@ -561,10 +674,60 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // ---- teardown: every role is done (or has drained after an abort)
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) {
+        // after an abort, give the copies and commits already issued for this
+        // CTA (some by the other CTA) time to land; then neither CTA leaves
+        // while the other may still use its shared memory or TMEM
+        if (threadIdx.x == 0 && *abort) sleep_ns(1000000);
+        cluster_sync();
+    }
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        tmem_dealloc<CG>(tmem_base, TMEM_COLS);
     }
+}
+
+using GemmKernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                           const CUtensorMap, const GemmArgs, const GemmArgs);
+
+// CTA-pair kernels: how many pairs can be resident at once (shared memory and
+// the GPCs' SM pairs decide), looked up once per kernel and device.
+constexpr int kMaxPairDevices = 64;
+std::atomic<int> g_pair_clusters[3][kMaxPairDevices];
+
+cudaError_t launch_pair(int slot, GemmKernel kern, const CUtensorMap& tmA, const CUtensorMap& tmB0,
+                        const CUtensorMap& tmB1, const GemmArgs& a, int num_sms, cudaStream_t s)
+{
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem_bytes<true>());
+    if (err != cudaSuccess) return err;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = smem_bytes<true>();
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int dev = 0;
+    err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxPairDevices) return cudaErrorInvalidDevice;
+    int clusters = g_pair_clusters[slot][dev].load(std::memory_order_relaxed);
+    if (clusters <= 0) {
+        cfg.gridDim = dim3((unsigned)(num_sms & ~1));
+        err = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+        if (err != cudaSuccess) return err;
+        if (clusters <= 0) return cudaErrorInvalidConfiguration;
+        g_pair_clusters[slot][dev].store(clusters, std::memory_order_relaxed);
+    }
+    clusters = clusters < num_sms / 2 ? clusters : num_sms / 2;
+    if (clusters <= 0) return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3((unsigned)(2 * clusters));
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB0, tmB1, tmB0, tmB0, a, a);
 }
 
 }  // namespace
@@ -579,28 +742,37 @@ cudaError_t launch_grouped_gemm_fused(int mode, const CUtensorMap& tmA, const CU
     if (a0.K % BK != 0) return cudaErrorInvalidValue;
     const bool fused = (mode == kFusedScatter || mode == kFusedCombine);
     if (fused && (a1.K % BK != 0 || a1.ready == nullptr)) return cudaErrorInvalidValue;
-    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap,
-                 const GemmArgs, const GemmArgs);
-    if (mode == kGemm0Gather) kern = grouped_gemm_kernel<kGemm0Gather>;
-    else if (mode == kGemm0Dense) kern = grouped_gemm_kernel<kGemm0Dense>;
-    else if (mode == kGemm1Scatter) kern = grouped_gemm_kernel<kGemm1Scatter>;
-    else if (mode == kGemm1Combine) kern = grouped_gemm_kernel<kGemm1Combine>;
-    else if (mode == kGemm0CpGather) kern = grouped_gemm_kernel<kGemm0CpGather>;
-    else if (mode == kFusedScatter) kern = grouped_gemm_kernel<kFusedScatter>;
-    else if (mode == kFusedCombine) kern = grouped_gemm_kernel<kFusedCombine>;
+    GemmKernel kern;
+    if (mode == kGemm0Gather) kern = grouped_gemm_kernel<kGemm0Gather, false>;
+    else if (mode == kGemm0Dense) kern = grouped_gemm_kernel<kGemm0Dense, false>;
+    else if (mode == kGemm1Scatter) kern = grouped_gemm_kernel<kGemm1Scatter, false>;
+    else if (mode == kGemm1Combine) kern = grouped_gemm_kernel<kGemm1Combine, false>;
+    else if (mode == kGemm0CpGather) kern = grouped_gemm_kernel<kGemm0CpGather, false>;
+    else if (mode == kFusedScatter) kern = grouped_gemm_kernel<kFusedScatter, false>;
+    else if (mode == kFusedCombine) kern = grouped_gemm_kernel<kFusedCombine, false>;
     else return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    constexpr size_t smem = smem_bytes<false>();
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    kern<<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tmA, tmB0, tmB1, tmA1, tmB2, a0, a1);
+    kern<<<num_sms, NUM_THREADS, smem, s>>>(tmA, tmB0, tmB1, tmA1, tmB2, a0, a1);
     return cudaGetLastError();
 }
 
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,
                                 const CUtensorMap& tmB1, const GemmArgs& a, int num_sms,
-                                cudaStream_t s)
+                                cudaStream_t s, int cta_group)
 {
     if (mode == kFusedScatter || mode == kFusedCombine) return cudaErrorInvalidValue;
-    return launch_grouped_gemm_fused(mode, tmA, tmB0, tmB1, tmB0, tmB0, a, a, num_sms, s);
+    if (cta_group == 1) return launch_grouped_gemm_fused(mode, tmA, tmB0, tmB1, tmB0, tmB0, a, a, num_sms, s);
+    if (cta_group != 2) return cudaErrorInvalidValue;
+    if (a.M == 0) return cudaSuccess;
+    if (a.G < 1 || a.G > MAX_GROUPS - 1 || a.K % BK != 0) return cudaErrorInvalidValue;
+    if (mode == kGemm0Dense) return launch_pair(0, grouped_gemm_kernel<kGemm0Dense, true>, tmA, tmB0, tmB1, a, num_sms, s);
+    if (mode == kGemm1Scatter)
+        return launch_pair(1, grouped_gemm_kernel<kGemm1Scatter, true>, tmA, tmB0, tmB1, a, num_sms, s);
+    if (mode == kGemm1Combine)
+        return launch_pair(2, grouped_gemm_kernel<kGemm1Combine, true>, tmA, tmB0, tmB1, a, num_sms, s);
+    return cudaErrorInvalidValue;   // the gathered-A GEMM0 forms run one CTA per MMA
 }
 
 }  // namespace moe

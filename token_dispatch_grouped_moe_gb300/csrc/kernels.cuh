@@ -111,9 +111,12 @@ struct GemmArgs {
 // [M,H] (box 64 x 128); kGemm1Scatter -> h [M,F] (box 64 x 128).
 // tmB0/tmB1: GEMM0 -> W1 / W3 viewed as [G*H, F]; GEMM1 -> W2 viewed as [G*F, H]
 // (tmB1 unused). All boxes 64 wide with 128-byte swizzle.
+// cta_group 2: one MMA of 256 x 256 over a CTA pair (a 2-CTA cluster), each
+// CTA staging half of A's rows and half of B's columns; kGemm0Dense,
+// kGemm1Scatter and kGemm1Combine only.
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,
                                 const CUtensorMap& tmB1, const GemmArgs& a, int num_sms,
-                                cudaStream_t s);
+                                cudaStream_t s, int cta_group = 1);
 // Both GEMMs in one launch: a0 / tmA, tmB0, tmB1 as for kGemm0Dense; a1 / tmA1
 // (h) and tmB2 (W2) as for GEMM1. mode is kFusedScatter or kFusedCombine.
 cudaError_t launch_grouped_gemm_fused(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,

@@ -1,5 +1,6 @@
-// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA (tiled and
-// gather4), tcgen05 (TMEM alloc, MMA, commit, ld) and a bounded wait.
+// ptx.cuh -- thin inline-PTX wrappers for sm_103a: cluster, mbarrier, TMA
+// (tiled and gather4), tcgen05 (TMEM alloc, MMA, commit, ld; one CTA or a CTA
+// pair) and a bounded wait.
 //
 // Every wait in this library is bounded: a wait that has not completed after
 // kWaitLimitNs of %globaltimer time records MOE_DEV_ERR_TIMEOUT in the
@@ -49,6 +50,38 @@ __device__ __forceinline__ uint32_t elect_one_sync()
     return pred;
 }
 
+// -------------------------------------------------------------- cluster --
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of the variable at shared::cta address `addr`
+// in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+// Every thread of every CTA of the cluster (all threads must call it).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                     "memory");
+}
+
+// Sleeps about `ns` nanoseconds (bounded by %globaltimer).
+__device__ __forceinline__ void sleep_ns(unsigned long long ns)
+{
+    const unsigned long long t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < ns) __nanosleep(1000);
+}
+
 // ------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
@@ -75,29 +108,49 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
         : "memory");
 }
 
+// Arrive on a barrier of another CTA of the cluster (`bar` from mapa_shared),
+// releasing this thread's prior writes at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// CLUSTER: acquire at cluster scope (the phase was completed by arrivals from
+// another CTA of the cluster).
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred P;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
-        "selp.b32 %0, 1, 0, P;\n\t}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if constexpr (CLUSTER)
+        asm volatile(
+            "{\n\t.reg .pred P;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P, [%1], %2;\n\t"
+            "selp.b32 %0, 1, 0, P;\n\t}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred P;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+            "selp.b32 %0, 1, 0, P;\n\t}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
 // Waits for the phase of `bar` with parity `parity`. Returns false (after
 // recording a timeout and raising *abort) if it does not complete within
 // kWaitLimitNs, or if another role of the CTA has already raised *abort.
+template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
                                           uint32_t* err)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
     unsigned long long t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait<CLUSTER>(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -164,6 +217,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// The same load issued by either CTA of a CTA pair: the box lands in this
+// CTA's shared memory and its bytes complete on `bar`, a shared::cluster
+// address that may be the pair's leader's barrier.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t c0, int32_t c1,
+                                                 uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
 // Gather of four rows r0..r3 (box one row high) starting at column c0; the
 // rows land one after another at dst.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t c0, int32_t r0,
@@ -178,22 +244,40 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int3
 
 // -------------------------------------------------------------- tcgen05 --
 
+// CG = 1: this CTA's tensor core and TMEM. CG = 2: a CTA pair (cluster ranks
+// 0 and 1); every tcgen05 instruction of a kernel uses one CG, and a pair's
+// alloc / relinquish / dealloc are issued by one warp in each of the two CTAs.
+template <int CG = 1>
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols)
 {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-                 "r"(ncols)
-                 : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+                     "r"(ncols)
+                     : "memory");
 }
 
+template <int CG = 1>
 __device__ __forceinline__ void tmem_relinquish()
 {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <int CG = 1>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
 {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+    if constexpr (CG == 2)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before()
@@ -207,23 +291,53 @@ __device__ __forceinline__ void tc_fence_after()
 }
 
 // D[tmem] (+)= A[smem desc] * B[smem desc], kind::f16 (bf16 in, f32 out).
+// CG = 2 (issued by the pair's rank-0 CTA): A is 2 x 128 rows, one half in
+// each CTA's shared memory at the same address; B's N columns are split the
+// same way (rank 0 holds the first N/2); each CTA's TMEM receives its 128 rows.
+template <int CG = 1>
 __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                            uint32_t idesc, uint32_t accumulate)
 {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
+    if constexpr (CG == 2)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+            "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+            : "memory");
 }
 
-// Arrive once on `bar` when every tcgen05 op issued so far by this thread is done.
+// Arrive once on `bar` when every tcgen05 op issued so far by this thread is
+// done. CG = 2: on the barrier at the same address in both CTAs of the pair.
+template <int CG = 1>
 __device__ __forceinline__ void tc_commit(uint32_t bar)
 {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
+    if constexpr (CG == 2) {
+        const uint16_t both = 3;
+        asm volatile(
+            "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+            " [%0], %1;" ::"r"(bar),
+            "h"(both)
+            : "memory");
+    } else {
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+            : "memory");
+    }
+}
+
+// CG = 2 form of a commit that arrives on this CTA's barrier only.
+__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tc_wait_ld()
@@ -279,10 +393,6 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
     return d;
 }
 
-// Instruction descriptor for kind::f16 with bf16 A and B, f32 accumulator.
-//   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format
-//   (1 = bf16); 15 A major (0 = K); 16 B major (1 = MN); 17-22 N >> 3;
-//   24-28 M >> 4.
 // The same for a K-major operand in 64-byte-swizzled rows (layout type 4):
 // 8-row groups sbo bytes apart (512 for dense 64-byte rows).
 __device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t addr, uint32_t lbo, uint32_t sbo)
@@ -295,6 +405,11 @@ __device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t addr, uint32_t lbo, 
     d |= (uint64_t)4 << 61;
     return d;
 }
+
+// Instruction descriptor for kind::f16 with bf16 A and B, f32 accumulator.
+//   bits 4-5 D format (1 = f32); 7-9 A format (1 = bf16); 10-12 B format
+//   (1 = bf16); 15 A major (0 = K); 16 B major (1 = MN); 17-22 N >> 3;
+//   24-28 M >> 4 (M = 256: a CTA pair, 128 rows in each CTA's TMEM).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn_major,
                                                       bool b_mn_major)
 {

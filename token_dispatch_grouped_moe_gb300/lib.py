@@ -38,6 +38,10 @@ OPT_GEMM_FUSION = 2
 GEMM_FUSION_AUTO = 0      # by shape (the library's table)
 GEMM_FUSION_ON = 1        # both routed GEMMs in one persistent launch
 GEMM_FUSION_OFF = 2       # two launches
+OPT_CTA_GROUP = 3
+CTA_GROUP_AUTO = 0        # by rows per expert (the library's table)
+CTA_GROUP_ONE = 1         # one CTA per 128 x 256 MMA tile
+CTA_GROUP_PAIR = 2        # a 2-CTA cluster per 256 x 256 MMA tile (tcgen05 cta_group::2)
 
 
 class MoeError(RuntimeError):
@@ -68,7 +72,8 @@ class RoutingOut(ctypes.Structure):
 
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("router", "gemm0_a", "combine", "gemm_fusion", "tile_m",
-                                              "tile_n", "tile_k", "stages", "cta_group")]
+                                              "tile_n", "tile_k", "stages", "cta_group",
+                                              "cta_group_gemm1")]
 
 
 ROUTER_STREAM, ROUTER_SLICED, ROUTER_CLUSTER, ROUTER_BLOCK = 0, 1, 2, 3
@@ -165,6 +170,15 @@ def set_gemm_fusion(mode: int) -> None:
 
 def get_gemm_fusion() -> int:
     return int(load().moe_get_option(OPT_GEMM_FUSION))
+
+
+def set_cta_group(mode: int) -> None:
+    """CTAs per MMA of the dense-A expert GEMMs (CTA_GROUP_AUTO / _ONE / _PAIR)."""
+    _ok(load().moe_set_option(OPT_CTA_GROUP, int(mode)), "moe_set_option")
+
+
+def get_cta_group() -> int:
+    return int(load().moe_get_option(OPT_CTA_GROUP))
 
 
 def selftest_wait_timeout(limit_ms: int = 200, stream=None) -> int:
