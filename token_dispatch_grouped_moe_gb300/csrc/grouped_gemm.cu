@@ -38,7 +38,7 @@
 //     same left fold as the separate combine kernel) and writes the bf16
 //     output. Which row is last depends on scheduling; the sum does not.
 //
-// Kernel shape: one CTA per SM (192 threads, ~197 KB of shared memory),
+// Kernel shape: one CTA per SM (224 threads, ~197 KB of shared memory),
 // persistent over a static schedule of (expert, N tile, M tile) work items
 // read from the device tile table (no host sync). Roles:
 //   warp 0      TMA producer: 4-stage ring of {A 128x64, B 64x256} bf16 tiles,
@@ -48,6 +48,15 @@
 //               accumulators in TMEM, double-buffered (2 x 256 columns) so the
 //               epilogue of one tile overlaps the main loop of the next.
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time.
+//   warp 6      cp.async row gather (kGemm0CpGather only).
+// CTA pairs (template argument PAIR; dense-A GEMM0 and GEMM1): a 2-CTA cluster
+// shares one tcgen05.mma.cta_group::2 of M=256 N=256 K=16. Each CTA stages its
+// 128 rows of A and half of B's columns (6 stages of 32 KB); both CTAs' TMA
+// boxes complete on the rank-0 CTA's stage barrier; rank 0 issues the MMAs and
+// its commits arrive on the barriers of both CTAs (multicast); the peer's
+// epilogue releases a TMEM buffer on rank 0's barrier. TMEM (512 columns) is
+// one collective allocation at the same address in both CTAs. Work items are
+// 256-row tiles; rank 0 takes the first 128 rows, rank 1 the rest.
 // Every wait is bounded (ptx.cuh); on a timeout the CTA drains what it
 // issued, frees its TMEM and exits with the error recorded.
 #include <atomic>
