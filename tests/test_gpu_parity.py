@@ -617,3 +617,43 @@ def test_full_config(lib, oracle, name):
     if c.zipf:
         share = r["routing"].counts.cpu().numpy() / c.R
         assert 0.38 <= share[0] <= 0.45
+
+
+@pytest.mark.parametrize("shape", [(1500, 512, 1408, 8, 2, 0), (2100, 448, 320, 4, 2, 640),
+                                   (300, 256, 192, 64, 6, 0)])
+def test_layer_in_cuda_graph(lib, shape):
+    """moe_layer_forward captured into a CUDA graph and replayed gives the same
+    bits as the eager call, also after the input changes in place: every
+    launch (the cooperative dispatch, the CTA-pair cluster launches, the
+    memsets) is stream-ordered, with no host synchronisation or allocation."""
+    T, H, F, E, k, Fs = shape
+    inp = make_inputs(T, H, F, E, Fs=Fs, seed=23)
+    g = {n: v.cuda() for n, v in inp.items()}
+    dims = lib.make_dims(T, H, F, E, k, Fs)
+    ws = lib.workspace(dims)
+    x = g["x"].clone()
+
+    def call(out=None):
+        return lib.layer_forward(dims, x, g["Wg"], g["W1"], g["W3"], g["W2"], ws, W1s=g.get("W1s"),
+                                 W3s=g.get("W3s"), W2s=g.get("W2s"), out=out)
+
+    eager = call().clone()
+    out = torch.empty_like(eager)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call(out)   # warm-up on the capture stream (attributes, occupancy look-ups)
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call(out)
+    out.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+    assert torch.equal(out, eager)
+    # new tokens in the same buffer: the replay routes and computes them afresh
+    x.copy_(make_inputs(T, H, F, E, Fs=Fs, seed=24, only=("x",))["x"].cuda())
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, call().clone())
