@@ -237,9 +237,11 @@ def bench_ours(args, cfg):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
+    launches0 = lib.launch_count()
     for i in range(args.steps):
         flush.fill_(1)
         step(recs[i][1])
+    launches = lib.launch_count() - launches0   # the library's own count of its kernels
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     if world > 1:
@@ -312,12 +314,7 @@ def bench_ours(args, cfg):
     stage_roofline["route"]["frac"] = round(stage_roofline["route"]["gbs"] / peaks["hbm_gbs"], 4)
 
     value = world * flops / (ms * 1e-3) / 1e12
-    # route (+ the top-k pass of the sliced router, E > 8); histogram, scatter,
-    # x_perm gather; GEMM0, GEMM1; shared GEMMs; a separate combine unless fused
     fused = plan.combine == lib.COMBINE_FUSED
-    route_launches = 2 if (cfg.E > 8 and cfg.E % 8 == 0) else 1
-    launches_per_step = (route_launches + 3 + (1 if fused_gemms else 2) + (2 if cfg.Fs else 0)
-                         + (0 if fused else 1))
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -354,7 +351,7 @@ def bench_ours(args, cfg):
         "e2e": {"value": round(world * flops / (e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": cfg.T * cfg.H * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.H * 2},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 4),
     }

@@ -213,6 +213,12 @@ moe_status moe_selftest_wait_timeout(int32_t limit_ms, moe_stream_t stream);
 /* Library version (major*10000 + minor*100 + patch). */
 int moe_version(void);
 
+/* Number of CUDA kernels this library has launched in this process (all
+ * threads, devices and streams) since it was loaded: each kernel launch of
+ * every call counts once; memsets and copies do not. A caller takes the
+ * difference around a region to count what that region launched. */
+uint64_t moe_launch_count(void);
+
 /* Text for a status code. Never null. */
 const char* moe_status_string(int status);
 

@@ -114,11 +114,14 @@ def test_options(L):
 
 
 def test_zero_tokens_is_noop_on_host(L):
-    """T = 0 returns MOE_OK before touching any pointer or the device."""
+    """T = 0 returns MOE_OK before touching any pointer or the device, and
+    launches nothing."""
     from token_dispatch_grouped_moe_gb300 import lib
     d = lib.make_dims(0, 64, 64, 8, 2)
+    n0 = lib.launch_count()
     assert L.moe_route(ctypes.byref(d), None, None, None, None, None, None) == 0
     assert L.moe_combine(ctypes.byref(d), None, 1, None, None) == 0
+    assert lib.launch_count() == n0
 
 
 def test_layer_plan_table(L):

@@ -657,3 +657,29 @@ def test_layer_in_cuda_graph(lib, shape):
     graph.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, call().clone())
+
+
+@pytest.mark.parametrize("shape,expected", [
+    # stream router, one cooperative dispatch launch, x_perm copy, both GEMMs in
+    # one launch (600 rows < 512 x 8), separate combine (F < 4096)
+    ((300, 256, 192, 8, 2, 0), 5),
+    # sliced router + top-k pass (E = 64), dispatch, copy, one GEMM launch, combine
+    ((300, 256, 192, 64, 6, 0), 6),
+    # + the shared expert's two GEMMs; two routed GEMM launches (1050 rows per expert)
+    ((2100, 448, 320, 4, 2, 640), 8),
+])
+def test_launch_count(lib, shape, expected):
+    """moe_launch_count counts exactly the kernels a layer call launches."""
+    T, H, F, E, k, Fs = shape
+    inp = make_inputs(T, H, F, E, Fs=Fs, seed=2)
+    g = {n: v.cuda() for n, v in inp.items()}
+    dims = lib.make_dims(T, H, F, E, k, Fs)
+    ws = lib.workspace(dims)
+    for _ in range(2):
+        n0 = lib.launch_count()
+        lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws, W1s=g.get("W1s"),
+                          W3s=g.get("W3s"), W2s=g.get("W2s"))
+        assert lib.launch_count() - n0 == expected
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+

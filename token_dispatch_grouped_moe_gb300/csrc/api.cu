@@ -16,7 +16,7 @@
 namespace moe {
 namespace {
 
-constexpr int kVersion = 100;   // 0.1.0
+constexpr int kVersion = 200;   // 0.2.0
 constexpr int kMaxDevices = 64;
 
 // ------------------------------------------------------------ device info --
@@ -26,6 +26,7 @@ std::atomic<int> g_gemm0_a{MOE_GEMM0_A_PERMUTED};
 std::atomic<int> g_combine{MOE_COMBINE_AUTO};
 std::atomic<int> g_gemm_fusion{MOE_GEMM_FUSION_AUTO};
 std::atomic<int> g_cta_group{MOE_CTA_GROUP_AUTO};
+std::atomic<unsigned long long> g_launch_count{0};
 
 int num_sms_current()
 {
@@ -346,6 +347,9 @@ void record(moe_event_t ev, cudaStream_t s)
 }
 
 }  // namespace
+
+void count_launch() { g_launch_count.fetch_add(1, std::memory_order_relaxed); }
+
 }  // namespace moe
 
 using namespace moe;
@@ -353,6 +357,8 @@ using namespace moe;
 extern "C" {
 
 int moe_version(void) { return kVersion; }
+
+uint64_t moe_launch_count(void) { return g_launch_count.load(std::memory_order_relaxed); }
 
 const char* moe_status_string(int status)
 {

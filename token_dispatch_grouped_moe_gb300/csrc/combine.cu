@@ -59,6 +59,7 @@ cudaError_t launch_combine(const float* slot, int32_t n_slots, uint16_t* out, in
     const int64_t cap = (int64_t)num_sms * 8;   // 8 resident blocks of 256 per SM
     if (blocks > cap) blocks = cap;
     combine_kernel<<<(int)blocks, kCombineThreads, 0, s>>>(slot, n_slots, out, TH);
+    count_launch();
     return cudaGetLastError();
 }
 

@@ -736,7 +736,9 @@ cudaError_t launch_pair(int slot, GemmKernel kern, const CUtensorMap& tmA, const
     clusters = clusters < num_sms / 2 ? clusters : num_sms / 2;
     if (clusters <= 0) return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3((unsigned)(2 * clusters));
-    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB0, tmB1, tmB0, tmB0, a, a);
+    err = cudaLaunchKernelEx(&cfg, kern, tmA, tmB0, tmB1, tmB0, tmB0, a, a);
+    if (err == cudaSuccess) count_launch();
+    return err;
 }
 
 }  // namespace
@@ -764,6 +766,7 @@ cudaError_t launch_grouped_gemm_fused(int mode, const CUtensorMap& tmA, const CU
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     kern<<<num_sms, NUM_THREADS, smem, s>>>(tmA, tmB0, tmB1, tmA1, tmB2, a0, a1);
+    count_launch();
     return cudaGetLastError();
 }
 

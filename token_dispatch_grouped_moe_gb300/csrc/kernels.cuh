@@ -124,6 +124,9 @@ cudaError_t launch_grouped_gemm_fused(int mode, const CUtensorMap& tmA, const CU
                                       const CUtensorMap& tmB2, const GemmArgs& a0, const GemmArgs& a1,
                                       int num_sms, cudaStream_t s);
 
+// Counts one kernel launch issued by this library (read with moe_launch_count).
+void count_launch();
+
 cudaError_t launch_combine(const float* slot, int32_t n_slots, uint16_t* out, int64_t T, int32_t H,
                            int num_sms, cudaStream_t s);
 

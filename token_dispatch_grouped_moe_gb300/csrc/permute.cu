@@ -242,6 +242,7 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s)
     if (n == 0) {
         // no assignments: zero counts/offsets/tile table via one tiny block
         perm_scatter_kernel<<<1, kScatterThreads, 0, s>>>(a, 0);
+        count_launch();
         return cudaGetLastError();
     }
     // one cooperative launch while every chunk's block can be resident at once
@@ -254,13 +255,17 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s)
         PermuteArgs args = a;
         int n_chunks = n;
         void* params[] = {&args, &n_chunks};
-        return cudaLaunchCooperativeKernel((const void*)perm_fused_kernel, dim3(n), dim3(kScatterThreads),
-                                           params, 0, s);
+        const cudaError_t e = cudaLaunchCooperativeKernel((const void*)perm_fused_kernel, dim3(n),
+                                                          dim3(kScatterThreads), params, 0, s);
+        if (e == cudaSuccess) count_launch();
+        return e;
     }
     perm_hist_kernel<<<n, kHistThreads, 0, s>>>(a);
+    count_launch();
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     perm_scatter_kernel<<<n, kScatterThreads, 0, s>>>(a, n);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -272,12 +277,14 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* src_row, const 
     const int64_t blocks_needed = (R + 7) / 8;
     const int grid = (int)(blocks_needed < (int64_t)num_sms * 8 ? blocks_needed : (int64_t)num_sms * 8);
     gather_rows_kernel<<<grid, 256, 0, s>>>(x, src_row, r_valid, x_perm, R, T, H, k, err);
+    count_launch();
     return cudaGetLastError();
 }
 
 cudaError_t launch_tile_table(const int32_t* offsets, int32_t G, int32_t* tile_start, cudaStream_t s)
 {
     tile_table_kernel<<<1, 256, 0, s>>>(offsets, G, tile_start);
+    count_launch();
     return cudaGetLastError();
 }
 

@@ -267,6 +267,7 @@ cudaError_t launch_route_t(const RouteArgs& a, int num_sms, cudaStream_t s)
     const int64_t groups = (a.T + (int64_t)kRouteWarps * NT - 1) / ((int64_t)kRouteWarps * NT);
     const int grid = (int)(groups < num_sms ? groups : num_sms);
     kern<<<grid, kRouteThreads, smem, s>>>(a, ms);
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -678,6 +679,7 @@ cudaError_t launch_cluster(const RouteArgs& a, int num_sms, cudaStream_t s)
     cfg.gridDim = dim3((unsigned)(clusters * S::CS));
     err = cudaLaunchKernelEx(&cfg, kern, a);
     if (err != cudaSuccess) return err;
+    count_launch();
     return cudaGetLastError();
 }
 
@@ -1104,6 +1106,7 @@ bool launch_stream(const RouteArgs& a, int num_sms, cudaStream_t s, cudaError_t&
     if (n_streams > G) n_streams = G;
     if (n_streams < 1) n_streams = 1;
     kern<<<(unsigned)(n_streams * n_sl), S::THREADS, smem, s>>>(gmap, xmap, a, gate_tma ? 1 : 0, n_sl);
+    count_launch();
     err = cudaGetLastError();
     if (err != cudaSuccess || n_sl == 1) return true;
     const unsigned blocks = (unsigned)((a.T + 31) / 32);   // 8 warps x 4 tokens
@@ -1115,6 +1118,7 @@ bool launch_stream(const RouteArgs& a, int num_sms, cudaStream_t s, cudaError_t&
         route_topk_kernel<16><<<blocks, 256, 0, s>>>(a);
     else
         route_topk_kernel<32><<<blocks, 256, 0, s>>>(a);
+    count_launch();
     err = cudaGetLastError();
     return true;
 }
@@ -1206,6 +1210,7 @@ cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* wsg, float* sc
     const int64_t blocks_needed = (T + 7) / 8;
     const int64_t cap = (int64_t)num_sms * 8;
     shared_gate_kernel<<<(int)(blocks_needed < cap ? blocks_needed : cap), 256, 0, s>>>(x, wsg, scale, T, H);
+    count_launch();
     return cudaGetLastError();
 }
 

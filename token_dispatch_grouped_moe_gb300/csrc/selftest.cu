@@ -32,6 +32,7 @@ extern "C" moe_status moe_selftest_wait_timeout(int32_t limit_ms, moe_stream_t s
     if (cudaMemcpyToSymbolAsync(g_selftest_err, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, s) != cudaSuccess)
         return MOE_ERR_CUDA;
     selftest_wait_kernel<<<1, 1, 0, s>>>((unsigned long long)limit_ms * 1000000ull);
+    moe::count_launch();
     if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemcpyFromSymbolAsync(&word, g_selftest_err, sizeof word, 0, cudaMemcpyDeviceToHost, s) !=
             cudaSuccess ||

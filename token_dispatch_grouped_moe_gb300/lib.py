@@ -24,7 +24,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_set_option",
            "moe_get_option", "moe_permute_static", "moe_route_ex", "moe_layer_forward_ex",
-           "moe_layer_plan", "moe_selftest_wait_timeout"]
+           "moe_layer_plan", "moe_selftest_wait_timeout", "moe_launch_count"]
 
 OPT_GEMM0_A = 0
 GEMM0_A_PERMUTED = 0      # dispatch copies token rows to x_perm; GEMM0 loads dense tiles
@@ -95,6 +95,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     D = ctypes.POINTER(Dims)
     lib.moe_version.restype = ctypes.c_int
     lib.moe_version.argtypes = []
+    lib.moe_launch_count.restype = ctypes.c_uint64
+    lib.moe_launch_count.argtypes = []
     lib.moe_status_string.restype = ctypes.c_char_p
     lib.moe_status_string.argtypes = [ctypes.c_int]
     lib.moe_workspace_size.restype = sz
@@ -179,6 +181,11 @@ def set_cta_group(mode: int) -> None:
 
 def get_cta_group() -> int:
     return int(load().moe_get_option(OPT_CTA_GROUP))
+
+
+def launch_count() -> int:
+    """Kernels this library has launched in this process so far."""
+    return int(load().moe_launch_count())
 
 
 def selftest_wait_timeout(limit_ms: int = 200, stream=None) -> int:
