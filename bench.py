@@ -6,8 +6,11 @@ A step is one whole layer forward (route -> permute -> GEMM0+SwiGLU ->
 GEMM1+scatter -> combine) over one batch of T tokens, through the C ABI
 (moe_layer_forward). Inputs are seeded synthetic bf16 tensors of the
 configuration's shape, resident in HBM before timing. L2 is flushed (a
-256 MiB write) between timed steps; each step is timed with CUDA events on
-the launching stream. Prints one JSON line (rank 0).
+256 MiB write) between timed steps; each step is timed with one pair of CUDA
+events on the launching stream and nothing recorded between its stages.
+A second pass of the same steps, with the library recording an event before
+every stage, gives the per-stage times and the GEMM0 roofline. Prints one JSON
+line (rank 0).
 
 Multi-GPU: the layer's tokens are independent, so N GPUs run N independent
 replicas of the workload (weak scaling, no collective on the data path);
@@ -230,7 +233,11 @@ def bench_ours(args, cfg):
     if lib.check(ws) != lib.MOE_OK:
         raise RuntimeError("device error during warm-up")
 
-    recs = [new_events() for _ in range(args.steps)]
+    # the timed region: K layer calls, each bracketed by one pair of events on
+    # the launching stream and nothing between its stages (an event recorded
+    # between two kernels costs the second one its launch overlap, about 5 us)
+    step_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
@@ -240,7 +247,9 @@ def bench_ours(args, cfg):
     launches0 = lib.launch_count()
     for i in range(args.steps):
         flush.fill_(1)
-        step(recs[i][1])
+        step_evs[i][0].record(stream)
+        step()
+        step_evs[i][1].record(stream)
     launches = lib.launch_count() - launches0   # the library's own count of its kernels
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
@@ -249,15 +258,25 @@ def bench_ours(args, cfg):
     clocks = sampler.stop()
     if lib.check(ws) != lib.MOE_OK:
         raise RuntimeError("device error during timing")
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in step_evs]
+    ms = max_over_ranks(float(np.sum(step_ms)) / args.steps, device)
 
+    # stage pass: the same K calls again, the library recording an event before
+    # every stage: the per-stage times and the GEMM0 roofline come from here
+    recs = [new_events() for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(1)
+        step(recs[i][1])
+    torch.cuda.synchronize()
+    if lib.check(ws) != lib.MOE_OK:
+        raise RuntimeError("device error during the stage pass")
     stage_ms = {n: [] for n in ("route", "permute", "gemm0", "gemm1", "shared", "combine")}
-    step_ms = []
     for evs, _ in recs:
         t = [evs[0].elapsed_time(e) for e in evs]
-        step_ms.append(t[-1])
         for j, n in enumerate(stage_ms):
             stage_ms[n].append(t[j + 1] - t[j])
-    ms = max_over_ranks(float(np.sum(step_ms)) / args.steps, device)
+    stage_step_ms = float(np.mean([evs[0].elapsed_time(evs[-1]) for evs, _ in recs]))
 
     # end to end through the C ABI with host buffers: x H2D, layer, out D2H
     x_host = inp["x"].pin_memory()
@@ -343,6 +362,9 @@ def bench_ours(args, cfg):
                      "traffic": None if fused_gemms else GEMM0_TRAFFIC.get((cfg.name, plan.cta_group)),
                      "traffic_unit": "bytes per launch",
                      "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"},
+        "timing": {"value": "K layer calls, one event pair each, no events between stages",
+                   "stage_ms": "a second pass of K calls with an event before every stage",
+                   "stage_pass_ms_per_step": round(stage_step_ms, 4)},
         "gemm_plan": {"cta_group": plan.cta_group, "cta_group_gemm1": plan.cta_group_gemm1,
                       "tile": [plan.tile_m, plan.tile_n, plan.tile_k],
                       "stages": plan.stages, "one_launch": fused_gemms, "combine_fused": fused},
