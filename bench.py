@@ -40,8 +40,9 @@ from token_dispatch_grouped_moe_gb300.configs import CONFIGS  # noqa: E402
 METRIC = "MoE layer fwd bf16 TFLOP/s & tokens/s on 1 GB300; % of tensor peak / HBM BW"
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM0 launch, from a
 # one-pass ncu capture of this benchmark at the configuration's full size, keyed by
-# (configuration, CTAs per MMA); kernels without such a capture report null
-GEMM0_TRAFFIC = {("mixtral", 1): 2014122496 + 457581312, ("mixtral", 2): 2467793920 + 462183168}
+# (configuration, CTAs per MMA, who fills x_perm); kernels without such a capture
+# report null
+GEMM0_TRAFFIC = {("mixtral", 1, "kernel"): 2014122496 + 457581312, ("mixtral", 2, "kernel"): 2467793920 + 462183168}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -202,6 +203,8 @@ def bench_ours(args, cfg):
                          "off": lib.GEMM_FUSION_OFF}[args.gemm_fusion])
     lib.set_cta_group({"auto": lib.CTA_GROUP_AUTO, "one": lib.CTA_GROUP_ONE,
                        "pair": lib.CTA_GROUP_PAIR}[args.cta_group])
+    lib.set_x_perm_copy({"auto": lib.X_PERM_COPY_AUTO, "inline": lib.X_PERM_COPY_INLINE,
+                         "kernel": lib.X_PERM_COPY_KERNEL}[args.x_perm_copy])
 
     inp, g = make_workload(cfg, device)
     dims = lib.make_dims(cfg.T, cfg.H, cfg.F, cfg.E, cfg.k, cfg.Fs)
@@ -359,7 +362,8 @@ def bench_ours(args, cfg):
                                                               else ")"),
                      "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": None if fused_gemms else GEMM0_TRAFFIC.get((cfg.name, plan.cta_group)),
+                     "traffic": None if fused_gemms else GEMM0_TRAFFIC.get(
+                         (cfg.name, plan.cta_group, {1: "inline", 2: "kernel"}.get(plan.x_perm_copy))),
                      "traffic_unit": "bytes per launch",
                      "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"},
         "timing": {"value": "K layer calls, one event pair each, no events between stages",
@@ -367,7 +371,8 @@ def bench_ours(args, cfg):
                    "stage_pass_ms_per_step": round(stage_step_ms, 4)},
         "gemm_plan": {"cta_group": plan.cta_group, "cta_group_gemm1": plan.cta_group_gemm1,
                       "tile": [plan.tile_m, plan.tile_n, plan.tile_k],
-                      "stages": plan.stages, "one_launch": fused_gemms, "combine_fused": fused},
+                      "stages": plan.stages, "one_launch": fused_gemms, "combine_fused": fused,
+                      "x_perm_copy": {1: "inline", 2: "kernel"}.get(plan.x_perm_copy)},
         "stage_ms": stage_summary,
         "stage_roofline": stage_roofline,
         "e2e": {"value": round(world * flops / (e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
@@ -450,6 +455,8 @@ def main():
                     help="both routed GEMMs in one persistent launch, or two launches")
     ap.add_argument("--cta-group", default="auto", choices=["auto", "one", "pair"],
                     help="CTAs per tensor-core MMA in the dense-A expert GEMMs")
+    ap.add_argument("--x-perm-copy", default="auto", choices=["auto", "inline", "kernel"],
+                    help="x_perm filled inside GEMM0 while it runs, or by a kernel before it")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--ref-tokens", type=int, default=64, help="oracle tokens per reference step")
     args = ap.parse_args()

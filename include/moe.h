@@ -160,7 +160,21 @@ enum {
     MOE_OPT_CTA_GROUP = 3,
     MOE_CTA_GROUP_AUTO = 0,
     MOE_CTA_GROUP_ONE = 1,
-    MOE_CTA_GROUP_PAIR = 2
+    MOE_CTA_GROUP_PAIR = 2,
+    /* Who copies the routed token rows into dispatch order (x_perm) when
+     * GEMM0 reads them from there (MOE_GEMM0_A_PERMUTED, two GEMM launches):
+     *   MOE_X_PERM_COPY_AUTO   (default) the table (see moe_layer_plan): the
+     *                          kernel, which measured as fast on GB300;
+     *   MOE_X_PERM_COPY_INLINE a spare warp of every GEMM0 CTA, while the
+     *                          GEMM runs: each 128-row tile is computed as
+     *                          soon as its rows are copied (counted per
+     *                          tile), so the copy overlaps the tensor work;
+     *   MOE_X_PERM_COPY_KERNEL a copy kernel before GEMM0.
+     * The same bytes either way: bit-identical. */
+    MOE_OPT_X_PERM_COPY = 4,
+    MOE_X_PERM_COPY_AUTO = 0,
+    MOE_X_PERM_COPY_INLINE = 1,
+    MOE_X_PERM_COPY_KERNEL = 2
 };
 
 /* Sets a library-wide option for later calls (all devices and threads).
@@ -195,6 +209,7 @@ typedef struct {
                             * and stages describe it */
     int32_t cta_group_gemm1; /* the same for the routed GEMM1 (a second launch; 1 when both
                               * GEMMs share one launch) */
+    int32_t x_perm_copy;   /* MOE_X_PERM_COPY_INLINE or _KERNEL; 0 when GEMM0 does not read x_perm */
 } moe_plan;
 
 /* Fills *plan for `dims` (host only: no device work, no launch). Returns

@@ -94,8 +94,8 @@ def test_options(L):
     assert lib.get_gemm0_a() == lib.GEMM0_A_TMA_GATHER
     lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
     assert L.moe_set_option(0, 7) == 1
-    assert L.moe_set_option(5, 0) == 1
-    assert L.moe_get_option(5) == -1
+    assert L.moe_set_option(6, 0) == 1
+    assert L.moe_get_option(6) == -1
     assert lib.get_combine() == lib.COMBINE_AUTO
     for mode in (lib.COMBINE_FUSED, lib.COMBINE_SEPARATE, lib.COMBINE_AUTO):
         lib.set_combine(mode)
@@ -111,6 +111,11 @@ def test_options(L):
         lib.set_cta_group(mode)
         assert lib.get_cta_group() == mode
     assert L.moe_set_option(3, 3) == 1
+    assert lib.get_x_perm_copy() == lib.X_PERM_COPY_AUTO
+    for mode in (lib.X_PERM_COPY_INLINE, lib.X_PERM_COPY_KERNEL, lib.X_PERM_COPY_AUTO):
+        lib.set_x_perm_copy(mode)
+        assert lib.get_x_perm_copy() == mode
+    assert L.moe_set_option(4, 3) == 1
 
 
 def test_zero_tokens_is_noop_on_host(L):
@@ -146,6 +151,8 @@ def test_layer_plan_table(L):
             router, combine, fusion, cg, cg1), name
         tile = (256, 256, 64, 6) if cg == 2 else (128, 256, 64, 4)
         assert (p.gemm0_a, p.tile_m, p.tile_n, p.tile_k, p.stages) == (lib.GEMM0_A_PERMUTED, *tile), name
+        # x_perm is filled by a copy kernel unless the option asks for the in-GEMM0 copy
+        assert p.x_perm_copy == lib.X_PERM_COPY_KERNEL, name
     # the CTA-group option overrides the table; a gather A path runs one CTA
     d = lib.make_dims(8192, 4096, 14336, 8, 2)
     try:
@@ -157,10 +164,18 @@ def test_layer_plan_table(L):
         lib.set_gemm_fusion(lib.GEMM_FUSION_OFF)
         assert (lib.layer_plan(small).cta_group, lib.layer_plan(small).cta_group_gemm1) == (2, 2)
         lib.set_cta_group(lib.CTA_GROUP_AUTO)
+        lib.set_x_perm_copy(lib.X_PERM_COPY_INLINE)
+        assert lib.layer_plan(d).x_perm_copy == lib.X_PERM_COPY_INLINE
+        lib.set_gemm_fusion(lib.GEMM_FUSION_ON)   # one launch: x_perm by the kernel
+        assert lib.layer_plan(small).x_perm_copy == lib.X_PERM_COPY_KERNEL
+        lib.set_gemm_fusion(lib.GEMM_FUSION_OFF)
+        lib.set_x_perm_copy(lib.X_PERM_COPY_AUTO)
         lib.set_gemm0_a(lib.GEMM0_A_TMA_GATHER)
         assert (lib.layer_plan(d).cta_group, lib.layer_plan(d).cta_group_gemm1) == (1, 2)
+        assert lib.layer_plan(d).x_perm_copy == 0   # GEMM0 gathers its rows: no x_perm
     finally:
         lib.set_cta_group(lib.CTA_GROUP_AUTO)
+        lib.set_x_perm_copy(lib.X_PERM_COPY_AUTO)
         lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
         lib.set_gemm0_a(lib.GEMM0_A_PERMUTED)
     # E not a multiple of 8, E > 64, a gate too large for the streaming router

@@ -431,6 +431,57 @@ def test_cta_pair_bit_identical(lib, shape):
         assert torch.equal(outs[0], o)
 
 
+@pytest.mark.parametrize("shape", PAIR_SHAPES)
+def test_x_perm_copy_bit_identical(lib, shape):
+    """x_perm filled by GEMM0's copy warps while the GEMM runs (each tile waits
+    for its rows) gives the same bits as a copy kernel before GEMM0, with one
+    CTA or a CTA pair per MMA, through the layer call and moe_expert_ffn."""
+    T, H, F, E, k, Fs = shape
+    inp = make_inputs(T, H, F, E, Fs=Fs, seed=29)
+    g = {n: v.cuda() for n, v in inp.items()}
+    dims = lib.make_dims(T, H, F, E, k, Fs)
+    ws = lib.workspace(dims)
+    outs, slots = [], []
+    try:
+        lib.set_gemm_fusion(lib.GEMM_FUSION_OFF)
+        for cg in (lib.CTA_GROUP_ONE, lib.CTA_GROUP_PAIR):
+            lib.set_cta_group(cg)
+            for copy in (lib.X_PERM_COPY_KERNEL, lib.X_PERM_COPY_INLINE, lib.X_PERM_COPY_INLINE):
+                lib.set_x_perm_copy(copy)
+                outs.append(lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws,
+                                              W1s=g.get("W1s"), W3s=g.get("W3s"),
+                                              W2s=g.get("W2s")).clone())
+                idx, w = lib.route(dims, g["x"], g["Wg"])
+                counts, offsets, src_row, inv_pos, _ = lib.permute(dims, idx, ws)
+                slot = torch.empty(k, T, H, dtype=torch.float32, device="cuda")
+                lib.expert_ffn(dims, g["x"], src_row, offsets, g["W1"], g["W3"], g["W2"], w, ws, slot=slot)
+                slots.append(slot)
+    finally:
+        lib.set_x_perm_copy(lib.X_PERM_COPY_AUTO)
+        lib.set_cta_group(lib.CTA_GROUP_AUTO)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+    for o in outs[1:]:
+        assert torch.equal(outs[0], o)
+    for sl in slots[1:]:
+        assert torch.equal(slots[0], sl)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "f_tail", "h_tail_e64", "k_eq_e", "shared", "one_token",
+                                  "seventeen", "e256"])
+def test_small_case_x_perm_inline(lib, oracle, name):
+    """Edge cases with x_perm filled inside GEMM0 (two GEMM launches), against the oracle."""
+    T, H, F, E, k, Fs = SMALL_CASES[name]
+    lib.set_gemm_fusion(lib.GEMM_FUSION_OFF)
+    lib.set_x_perm_copy(lib.X_PERM_COPY_INLINE)
+    try:
+        run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=8, tol="elementwise")
+    finally:
+        lib.set_x_perm_copy(lib.X_PERM_COPY_AUTO)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
+
+
 @pytest.mark.parametrize("name", ["tiny", "ragged", "f_tail", "h_tail_e64", "dense_e1", "shared",
                                   "one_token", "e256"])
 def test_small_case_cta_pair(lib, oracle, name):

@@ -26,6 +26,7 @@ std::atomic<int> g_gemm0_a{MOE_GEMM0_A_PERMUTED};
 std::atomic<int> g_combine{MOE_COMBINE_AUTO};
 std::atomic<int> g_gemm_fusion{MOE_GEMM_FUSION_AUTO};
 std::atomic<int> g_cta_group{MOE_CTA_GROUP_AUTO};
+std::atomic<int> g_x_perm_copy{MOE_X_PERM_COPY_AUTO};
 std::atomic<unsigned long long> g_launch_count{0};
 
 int num_sms_current()
@@ -158,6 +159,12 @@ moe_plan plan_of(const moe_dims& d)
     p.cta_group = (p.gemm0_a == MOE_GEMM0_A_PERMUTED && !fuse)
                       ? cta_group_for(d.T * (int64_t)d.k, d.E, false) : 1;
     p.cta_group_gemm1 = fuse ? 1 : cta_group_for(d.T * (int64_t)d.k, d.E, true);
+    if (p.gemm0_a == MOE_GEMM0_A_PERMUTED) {
+        const int opt = g_x_perm_copy.load();
+        // measured no faster inline (the copy's bulk loads share each SM's TMA
+        // unit with the GEMM's operand loads): the kernel unless asked
+        p.x_perm_copy = (!fuse && opt == MOE_X_PERM_COPY_INLINE) ? MOE_X_PERM_COPY_INLINE : MOE_X_PERM_COPY_KERNEL;
+    }
     p.tile_m = p.cta_group == 2 ? 2 * kTileM : kTileM;
     p.tile_n = 256;
     p.tile_k = 64;
@@ -272,7 +279,7 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
                             uint16_t* h, uint32_t* err, int sms, cudaStream_t s, moe_event_t ev_mid,
                             const FusedCombine& fc = FusedCombine{false, 0, 0, nullptr, nullptr},
                             bool cp_gather = false, int32_t* ready = nullptr, int cta_group0 = 1,
-                            int cta_group1 = 1)
+                            int cta_group1 = 1, int32_t* copy_ready = nullptr, uint16_t* copy_dst = nullptr)
 {
     if (M == 0) {
         if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
@@ -323,8 +330,17 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
         if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
         return MOE_OK;
     }
+    if (copy_ready) {
+        // GEMM0's copy warps fill x_perm (copy_dst) from x while the GEMM runs
+        if (!dense || !src_row || !tile_start || !copy_dst) return MOE_ERR_INVALID_ARG;
+        MOE_TRY(cudaMemsetAsync(copy_ready, 0, (size_t)((M + kTileM - 1) / kTileM + G + 1) * 4, s));
+        a.copy_ready = copy_ready;
+        a.copy_dst = copy_dst;
+    }
     MOE_TRY(launch_grouped_gemm(dense ? kGemm0Dense : cp_gather ? kGemm0CpGather : kGemm0Gather, mx, m1,
                                 m3, a, sms, s, dense ? cta_group0 : 1));
+    a.copy_ready = nullptr;
+    a.copy_dst = nullptr;
     if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
     // GEMM1 + weighted scatter: h [rows, F] x W2 [F, H] -> slot[rank][token]
     a.N = d.H;
@@ -401,6 +417,12 @@ moe_status moe_set_option(int option, int value)
         g_cta_group.store(value);
         return MOE_OK;
     }
+    if (option == MOE_OPT_X_PERM_COPY) {
+        if (value != MOE_X_PERM_COPY_AUTO && value != MOE_X_PERM_COPY_INLINE && value != MOE_X_PERM_COPY_KERNEL)
+            return MOE_ERR_INVALID_ARG;
+        g_x_perm_copy.store(value);
+        return MOE_OK;
+    }
     return MOE_ERR_INVALID_ARG;
 }
 
@@ -410,6 +432,7 @@ int moe_get_option(int option)
     if (option == MOE_OPT_COMBINE) return g_combine.load();
     if (option == MOE_OPT_GEMM_FUSION) return g_gemm_fusion.load();
     if (option == MOE_OPT_CTA_GROUP) return g_cta_group.load();
+    if (option == MOE_OPT_X_PERM_COPY) return g_x_perm_copy.load();
     return -1;
 }
 
@@ -512,6 +535,10 @@ moe_status moe_expert_ffn(const moe_dims* dims, const moe_bf16* x, const int32_t
     const int32_t R = (int32_t)(dims->T * dims->k);
     const uint16_t* x_rows = nullptr;
     const int a_opt = g_gemm0_a.load();
+    // the layer's table decides whether both GEMMs share one launch (dense A)
+    // and who copies x_perm
+    const moe_plan plan = plan_of(*dims);
+    uint16_t* copy_dst = nullptr;
     if (a_opt == MOE_GEMM0_A_CP_GATHER && !src_row && dims->k == 1) {
         x_rows = x;   // identity dispatch: x is already in dispatch order
     } else if (a_opt == MOE_GEMM0_A_PERMUTED) {
@@ -519,13 +546,14 @@ moe_status moe_expert_ffn(const moe_dims* dims, const moe_bf16* x, const int32_t
             x_rows = x;   // identity dispatch: x is already in dispatch order
         } else {
             uint16_t* xp = reinterpret_cast<uint16_t*>(bytes(ws) + L.xp);
-            MOE_TRY(launch_gather_rows(x, src_row, offsets ? offsets + dims->E : nullptr, xp, R,
-                                       dims->T, dims->H, dims->k, err, sms, s));
+            if (plan.x_perm_copy == MOE_X_PERM_COPY_INLINE && src_row && tile)
+                copy_dst = xp;   // GEMM0's copy warps fill it
+            else
+                MOE_TRY(launch_gather_rows(x, src_row, offsets ? offsets + dims->E : nullptr, xp, R,
+                                           dims->T, dims->H, dims->k, err, sms, s));
             x_rows = xp;
         }
     }
-    // the layer's table decides whether both GEMMs share one launch (dense A)
-    const moe_plan plan = plan_of(*dims);
     const bool fuse_gemms = x_rows && plan.gemm_fusion == MOE_GEMM_FUSION_ON;
     MOE_TRY_STATUS(run_expert_gemms(*dims, R, dims->F, dims->E, dims->k, x, x_rows, src_row, tile,
                                     offsets, W1, W3, W2, topk_w, slot,
@@ -533,7 +561,9 @@ moe_status moe_expert_ffn(const moe_dims* dims, const moe_bf16* x, const int32_t
                                     nullptr, FusedCombine{false, 0, 0, nullptr, nullptr},
                                     a_opt == MOE_GEMM0_A_CP_GATHER,
                                     fuse_gemms ? reinterpret_cast<int32_t*>(bytes(ws) + L.ready) : nullptr,
-                                    plan.cta_group, plan.cta_group_gemm1));
+                                    plan.cta_group, plan.cta_group_gemm1,
+                                    copy_dst ? reinterpret_cast<int32_t*>(bytes(ws) + L.ready) : nullptr,
+                                    copy_dst));
     return finish(cudaSuccess, ws, s);
 }
 
@@ -621,7 +651,9 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     const bool permuted = (plan.gemm0_a == MOE_GEMM0_A_PERMUTED);
     const bool cp_gather = (plan.gemm0_a == MOE_GEMM0_A_CP_GATHER);
     uint16_t* xp = reinterpret_cast<uint16_t*>(w + L.xp);
-    if (permuted)
+    // x_perm: copied by GEMM0's copy warps while it runs, or by a kernel first
+    const bool copy_inline = permuted && plan.x_perm_copy == MOE_X_PERM_COPY_INLINE;
+    if (permuted && !copy_inline)
         MOE_TRY(launch_gather_rows(x, src, offsets + d.E, xp, R, d.T, d.H, d.k, err, sms, s));
 
     // both routed GEMMs in one launch (dense A only)
@@ -635,7 +667,9 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                                     // with a shared expert, only its GEMM1 (the last) combines
                                     FusedCombine{fused && d.F_shared == 0, 0, n_slots, arrive, out}, cp_gather,
                                     fuse_gemms ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr,
-                                    plan.cta_group, plan.cta_group_gemm1));
+                                    plan.cta_group, plan.cta_group_gemm1,
+                                    copy_inline ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr,
+                                    copy_inline ? xp : nullptr));
 
     record(events ? events->before_shared : nullptr, s);
     if (d.F_shared > 0) {

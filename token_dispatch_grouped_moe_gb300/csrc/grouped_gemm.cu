@@ -82,6 +82,8 @@ constexpr int NUM_THREADS = 224;   // 7 warps: TMA, MMA, 4 x epilogue, row gathe
 constexpr int GATHER_LAG = 2;      // stages a gathered A tile is given to land
 constexpr int MAX_GROUPS = 257;
 constexpr int TMEM_COLS = 512;
+constexpr int COPY_PIECE = 4096;   // dispatch copy: bytes per piece of a row
+constexpr int COPY_SLOTS = 6;      // dispatch copy: pieces in flight per CTA
 
 // One CTA per MMA (PAIR false): a stage holds A 128 x BK and all BN columns of
 // B. A CTA pair (PAIR true, tcgen05 cta_group::2): one MMA of 256 x BN over
@@ -109,13 +111,21 @@ struct SmemTail {
     int tile_start[MAX_GROUPS + 1];
     int offsets[MAX_GROUPS + 1];
     int tok[BM];                      // kGemm0CpGather: token of each row of the current tile
+    int tile128[MAX_GROUPS + 1];      // first 128-row tile of each group (the copy counters' index)
+    uint64_t cbar[COPY_SLOTS];        // dispatch copy: one barrier per ring slot
 };
 
+// The dispatch copy's ring follows the tail, 128-byte aligned.
 template <bool PAIR>
-constexpr size_t smem_bytes()
+__host__ __device__ constexpr size_t ring_offset()
 {
-    return 1024 /*align slack*/ + (size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES +
-           sizeof(SmemTail<Cfg<PAIR>::STAGES>);
+    return ((size_t)Cfg<PAIR>::STAGES * Cfg<PAIR>::STAGE_BYTES + sizeof(SmemTail<Cfg<PAIR>::STAGES>) + 127) &
+           ~(size_t)127;
+}
+template <bool PAIR>
+__host__ __device__ constexpr size_t smem_bytes()
+{
+    return 1024 /*align slack*/ + ring_offset<PAIR>() + (size_t)COPY_SLOTS * COPY_PIECE;
 }
 static_assert(smem_bytes<false>() <= 227 * 1024 && smem_bytes<true>() <= 227 * 1024, "shared memory");
 
@@ -197,6 +207,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             mbar_init(smem_u32(&st->tempty[a]), PAIR ? 8 : 4);
         }
         mbar_init(smem_u32(&st->drain), 1);
+        for (int c = 0; c < COPY_SLOTS; ++c) mbar_init(smem_u32(&st->cbar[c]), 1);
         st->abort = 0;
         fence_barrier_init();
     }
@@ -207,9 +218,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (lane == 0) {
                     st->offsets[0] = 0;
                     st->offsets[1] = args.M;
+                    st->tile128[0] = 0;
+                    st->tile128[1] = (args.M + BM - 1) / BM;
                 }
             } else {
-                for (int i = lane; i <= G; i += 32) st->offsets[i] = args.offsets[i];
+                for (int i = lane; i <= G; i += 32) {
+                    st->offsets[i] = args.offsets[i];
+                    st->tile128[i] = args.tile_start[i];
+                }
             }
             __syncwarp();
             const int per = (G + 31) / 32;
@@ -237,14 +253,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     } else if (args.tile_start == nullptr) {
         if (threadIdx.x == 0) {
-            st->tile_start[0] = 0;
-            st->tile_start[1] = (args.M + BM - 1) / BM;
+            st->tile_start[0] = st->tile128[0] = 0;
+            st->tile_start[1] = st->tile128[1] = (args.M + BM - 1) / BM;
             st->offsets[0] = 0;
             st->offsets[1] = args.M;
         }
     } else {
         for (int i = threadIdx.x; i <= G; i += blockDim.x) {
-            st->tile_start[i] = args.tile_start[i];
+            st->tile_start[i] = st->tile128[i] = args.tile_start[i];
             st->offsets[i] = args.offsets[i];
         }
     }
@@ -315,6 +331,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     tok[r] = t;
                 }
+            }
+            if (MODE == kGemm0Dense && args.copy_ready != nullptr && wk.rows > 0) {
+                // this tile's A rows come from the launch's copy warps: wait until
+                // every piece of them is counted, then read them through TMA
+                const int mt = st->tile128[wk.g] + (wk.row0 - st->offsets[wk.g]) / BM;
+                const int ppr = (args.K * 2 + COPY_PIECE - 1) / COPY_PIECE;
+                bool ready = true;
+                if (lane == 0) ready = wait_count(args.copy_ready + mt, wk.rows * ppr, abort, args.err);
+                if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) asm volatile("fence.proxy.async.global;" ::: "memory");
+                __syncwarp();
             }
             const int b_row = wk.g * (p1 ? args1.K : args.K);
             for (int kb = 0; kb < k_blocks; ++kb) {
@@ -513,6 +543,100 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // the last stages (and, after an abort, whatever is in flight)
             asm volatile("cp.async.wait_group 0;" ::: "memory");
             while (pending > 0) publish_oldest();
+        } else if (MODE == kGemm0Dense && args.copy_ready != nullptr) {
+            // ===================== dispatch copy: x -> x_perm =====================
+            // The rows of x_perm in 4 KB pieces, piece p = (row, part) taken by
+            // CTA p mod gridDim.x, so every CTA works from the first rows on and
+            // the first experts' tiles are ready first. A piece arrives in a
+            // ring slot by a bulk copy, goes out with 16-byte stores, and is
+            // counted on its 128-row tile after a proxy fence (the tile is read
+            // back through TMA).
+            unsigned char* ring = tiles + ring_offset<PAIR>();
+            const uint32_t ring_addr = smem_u32(ring);
+            const int64_t rows = st->offsets[G];            // rows with a valid expert
+            const int row_bytes = args.K * 2;
+            const int ppr = (row_bytes + COPY_PIECE - 1) / COPY_PIECE;
+            const int64_t total = rows * ppr;
+            const int64_t first = blockIdx.x, stride = gridDim.x;
+            auto piece = [&](int64_t j, int64_t& r, int& part, int& bytes) {
+                const int64_t p = first + j * stride;
+                r = p / ppr;
+                part = (int)(p - r * ppr);
+                bytes = min(COPY_PIECE, row_bytes - part * COPY_PIECE);
+                return p < total;
+            };
+            auto issue = [&](int64_t j) {
+                int64_t r;
+                int part, bytes;
+                if (!piece(j, r, part, bytes) || lane != 0) return;
+                const int f = args.src_row[r];
+                int64_t t = f / args.k;
+                if (f < 0 || t >= args.T) {
+                    report_error(args.err, MOE_DEV_ERR_BOUNDS);
+                    t = 0;
+                }
+                const int slot = (int)(j % COPY_SLOTS);
+                const uint32_t bar = smem_u32(&st->cbar[slot]);
+                mbar_arrive_expect_tx(bar, (uint32_t)bytes);
+                bulk_load(ring_addr + slot * COPY_PIECE,
+                          args.x + t * args.K + (int64_t)part * (COPY_PIECE / 2), (uint32_t)bytes, bar);
+            };
+            for (int q = 0; q < COPY_SLOTS; ++q) issue(q);
+            // counts the pieces j0 .. j-1 (copied, not yet counted) on their tiles,
+            // after one fence for all of them: lane q takes piece j0 + q
+            int64_t j0 = 0;
+            auto publish = [&](int64_t j_end) {
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                __threadfence();
+                __syncwarp();
+                int64_t r;
+                int part, bytes;
+                if (j0 + lane < j_end && piece(j0 + lane, r, part, bytes)) {
+                    int lo = 0, hi = G;   // the group of row r: offsets[lo] <= r < offsets[lo + 1]
+                    while (hi - lo > 1) {
+                        const int mid = (lo + hi) >> 1;
+                        if (st->offsets[mid] <= r) lo = mid; else hi = mid;
+                    }
+                    atomicAdd(args.copy_ready + st->tile128[lo] + (int)((r - st->offsets[lo]) / BM), 1);
+                }
+                j0 = j_end;
+            };
+            int64_t j = 0;
+            for (;; ++j) {
+                int64_t r;
+                int part, bytes;
+                if (!piece(j, r, part, bytes)) break;
+                const int slot = (int)(j % COPY_SLOTS);
+                const uint32_t parity = (uint32_t)((j / COPY_SLOTS) & 1);
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&st->cbar[slot]), parity, abort, args.err)))
+                    break;
+                // the piece into registers (at most 4 KB: 8 x 16 bytes a lane), the
+                // slot refilled at once, then the stores
+                const uint4* src = reinterpret_cast<const uint4*>(ring + slot * COPY_PIECE);
+                const int n16 = bytes / 16;
+                uint4 v[COPY_PIECE / 512];
+#pragma unroll
+                for (int u = 0; u < COPY_PIECE / 512; ++u)
+                    if (lane + 32 * u < n16) v[u] = src[lane + 32 * u];
+                __syncwarp();
+                if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(j + COPY_SLOTS);
+                uint4* dst = reinterpret_cast<uint4*>(args.copy_dst + r * args.K + (int64_t)part * (COPY_PIECE / 2));
+#pragma unroll
+                for (int u = 0; u < COPY_PIECE / 512; ++u)
+                    if (lane + 32 * u < n16) dst[lane + 32 * u] = v[u];
+                if (j + 1 - j0 == COPY_SLOTS) publish(j + 1);
+            }
+            publish(j);   // the last pieces (after an abort: those copied before it)
+            // after an abort: the pieces still in flight land before the CTA exits
+            if (lane == 0) {
+                for (int64_t q = j; q < j + COPY_SLOTS; ++q) {
+                    int64_t r;
+                    int part, bytes;
+                    if (!piece(q, r, part, bytes)) break;
+                    mbar_wait_drain(smem_u32(&st->cbar[q % COPY_SLOTS]), (uint32_t)((q / COPY_SLOTS) & 1));
+                }
+            }
         }
     } else {
         // ============================== epilogue ==============================
@@ -753,6 +877,9 @@ cudaError_t launch_grouped_gemm_fused(int mode, const CUtensorMap& tmA, const CU
     if (a0.K % BK != 0) return cudaErrorInvalidValue;
     const bool fused = (mode == kFusedScatter || mode == kFusedCombine);
     if (fused && (a1.K % BK != 0 || a1.ready == nullptr)) return cudaErrorInvalidValue;
+    // the in-launch dispatch copy: dense GEMM0 over a routed tile table only
+    if (a0.copy_ready && (mode != kGemm0Dense || !a0.copy_dst || !a0.src_row || !a0.tile_start || !a0.x))
+        return cudaErrorInvalidValue;
     GemmKernel kern;
     if (mode == kGemm0Gather) kern = grouped_gemm_kernel<kGemm0Gather, false>;
     else if (mode == kGemm0Dense) kern = grouped_gemm_kernel<kGemm0Dense, false>;
@@ -779,6 +906,8 @@ cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensor
     if (cta_group != 2) return cudaErrorInvalidValue;
     if (a.M == 0) return cudaSuccess;
     if (a.G < 1 || a.G > MAX_GROUPS - 1 || a.K % BK != 0) return cudaErrorInvalidValue;
+    if (a.copy_ready && (mode != kGemm0Dense || !a.copy_dst || !a.src_row || !a.tile_start || !a.x))
+        return cudaErrorInvalidValue;
     if (mode == kGemm0Dense) return launch_pair(0, grouped_gemm_kernel<kGemm0Dense, true>, tmA, tmB0, tmB1, a, num_sms, s);
     if (mode == kGemm1Scatter)
         return launch_pair(1, grouped_gemm_kernel<kGemm1Scatter, true>, tmA, tmB0, tmB1, a, num_sms, s);

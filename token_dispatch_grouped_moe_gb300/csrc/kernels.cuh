@@ -103,6 +103,12 @@ struct GemmArgs {
     uint16_t* out;               // kGemm1Combine: [T, N] bf16 layer output
     int32_t* ready;              // fused, GEMM1 args: [M tiles] count of GEMM0 warps done, zero first
     int32_t ready_target;        // fused, GEMM1 args: count that makes an M tile's h complete
+    // kGemm0Dense with the dispatch copy inside the launch (copy_ready non-null):
+    // warp 6 copies row r of x_perm from x[src_row[r] / k] for the rows
+    // r < offsets[G], in 4 KB pieces, counting each finished piece on its
+    // 128-row tile; the producer loads a tile once all its pieces are counted
+    uint16_t* copy_dst;          // x_perm [M, K], the A operand of this launch
+    int32_t* copy_ready;         // [128-row tiles] pieces copied, zero before the launch
     uint32_t* err;
 };
 

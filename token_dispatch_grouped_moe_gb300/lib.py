@@ -42,6 +42,10 @@ OPT_CTA_GROUP = 3
 CTA_GROUP_AUTO = 0        # by rows per expert (the library's table)
 CTA_GROUP_ONE = 1         # one CTA per 128 x 256 MMA tile
 CTA_GROUP_PAIR = 2        # a 2-CTA cluster per 256 x 256 MMA tile (tcgen05 cta_group::2)
+OPT_X_PERM_COPY = 4
+X_PERM_COPY_AUTO = 0      # by the library's table
+X_PERM_COPY_INLINE = 1    # GEMM0's copy warps fill x_perm while the GEMM runs
+X_PERM_COPY_KERNEL = 2    # a copy kernel before GEMM0
 
 
 class MoeError(RuntimeError):
@@ -73,7 +77,7 @@ class RoutingOut(ctypes.Structure):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("router", "gemm0_a", "combine", "gemm_fusion", "tile_m",
                                               "tile_n", "tile_k", "stages", "cta_group",
-                                              "cta_group_gemm1")]
+                                              "cta_group_gemm1", "x_perm_copy")]
 
 
 ROUTER_STREAM, ROUTER_SLICED, ROUTER_CLUSTER, ROUTER_BLOCK = 0, 1, 2, 3
@@ -181,6 +185,15 @@ def set_cta_group(mode: int) -> None:
 
 def get_cta_group() -> int:
     return int(load().moe_get_option(OPT_CTA_GROUP))
+
+
+def set_x_perm_copy(mode: int) -> None:
+    """Who fills x_perm for GEMM0 (X_PERM_COPY_AUTO / _INLINE / _KERNEL)."""
+    _ok(load().moe_set_option(OPT_X_PERM_COPY, int(mode)), "moe_set_option")
+
+
+def get_x_perm_copy() -> int:
+    return int(load().moe_get_option(OPT_X_PERM_COPY))
 
 
 def launch_count() -> int:
