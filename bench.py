@@ -42,7 +42,7 @@ METRIC = "MoE layer fwd bf16 TFLOP/s & tokens/s on 1 GB300; % of tensor peak / H
 # one-pass ncu capture of this benchmark at the configuration's full size, keyed by
 # (configuration, CTAs per MMA, who fills x_perm); kernels without such a capture
 # report null
-GEMM0_TRAFFIC = {("mixtral", 1, "kernel"): 2014122496 + 457581312, ("mixtral", 2, "kernel"): 2467793920 + 462183168}
+GEMM0_TRAFFIC = {("mixtral", 1, "kernel"): 2014122496 + 457581312, ("mixtral", 2, "kernel"): 2657268736 + 462815744}
 L2_FLUSH_BYTES = 256 << 20
 
 

@@ -734,3 +734,51 @@ def test_launch_count(lib, shape, expected):
     torch.cuda.synchronize()
     assert lib.check(ws) == lib.MOE_OK
 
+
+
+def _random_shapes(n, seed=2026):
+    """Seeded ragged shapes: T up to 3000 tokens, H and F multiples of 64 (so N
+    tails of 64 and 192 occur), E from 1 to 96, k up to min(E, 8), a shared
+    expert one time in three."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for _ in range(n):
+        E = int(rng.choice([1, 2, 3, 5, 8, 12, 16, 40, 64, 96]))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        T = int(rng.choice([1, 7, 130, 600, 1500, 3000]))
+        H = 64 * int(rng.integers(1, 17))
+        F = 64 * int(rng.integers(1, 25))
+        Fs = 64 * int(rng.integers(1, 9)) if rng.random() < 1 / 3 else 0
+        shapes.append((T, H, F, E, k, Fs))
+    return shapes
+
+
+@pytest.mark.parametrize("shape", _random_shapes(12))
+def test_random_shapes_all_paths(lib, oracle, shape):
+    """Every combination of the layer's path options on seeded ragged shapes:
+    CTA group (one / pair), GEMMs in one launch or two, x_perm copy (kernel /
+    inside GEMM0), combine (fused / separate) give the same bits; the default
+    path is within the arithmetic bound of the oracle."""
+    T, H, F, E, k, Fs = shape
+    res = run_case(lib, oracle, T, H, F, E, k, Fs=Fs, seed=31, tol="elementwise")
+    dims, ws, g = res["dims"], res["ws"], res["inputs"]
+    ref = res["out"].clone()
+    try:
+        for fusion in (lib.GEMM_FUSION_ON, lib.GEMM_FUSION_OFF):
+            lib.set_gemm_fusion(fusion)
+            for cg in (lib.CTA_GROUP_ONE, lib.CTA_GROUP_PAIR):
+                lib.set_cta_group(cg)
+                for copy in (lib.X_PERM_COPY_KERNEL, lib.X_PERM_COPY_INLINE):
+                    lib.set_x_perm_copy(copy)
+                    for combine in (lib.COMBINE_SEPARATE, lib.COMBINE_FUSED):
+                        lib.set_combine(combine)
+                        out = lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws,
+                                                W1s=g.get("W1s"), W3s=g.get("W3s"), W2s=g.get("W2s"))
+                        torch.cuda.synchronize()
+                        assert lib.check(ws) == lib.MOE_OK
+                        assert torch.equal(out, ref), (fusion, cg, copy, combine)
+    finally:
+        lib.set_combine(lib.COMBINE_AUTO)
+        lib.set_x_perm_copy(lib.X_PERM_COPY_AUTO)
+        lib.set_cta_group(lib.CTA_GROUP_AUTO)
+        lib.set_gemm_fusion(lib.GEMM_FUSION_AUTO)
