@@ -38,7 +38,7 @@
 //     same left fold as the separate combine kernel) and writes the bf16
 //     output. Which row is last depends on scheduling; the sum does not.
 //
-// Kernel shape: one CTA per SM (224 threads, ~197 KB of shared memory),
+// Kernel shape: one CTA per SM (224 threads, ~221 KB of shared memory),
 // persistent over a static schedule of (expert, N tile, M tile) work items
 // read from the device tile table (no host sync). Roles:
 //   warp 0      TMA producer: 4-stage ring of {A 128x64, B 64x256} bf16 tiles,
@@ -48,7 +48,10 @@
 //               accumulators in TMEM, double-buffered (2 x 256 columns) so the
 //               epilogue of one tile overlaps the main loop of the next.
 //   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns at a time.
-//   warp 6      cp.async row gather (kGemm0CpGather only).
+//   warp 6      cp.async row gather (kGemm0CpGather), or the dispatch copy
+//               x -> x_perm inside a kGemm0Dense launch (copy_ready set): 4 KB
+//               pieces through a 6-slot shared-memory ring, counted per
+//               128-row tile; the producer waits for a tile's count.
 // CTA pairs (template argument PAIR; dense-A GEMM0 and GEMM1): a 2-CTA cluster
 // shares one tcgen05.mma.cta_group::2 of M=256 N=256 K=16. Each CTA stages its
 // 128 rows of A and half of B's columns (6 stages of 32 KB); both CTAs' TMA
