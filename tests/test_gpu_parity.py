@@ -670,6 +670,16 @@ def test_full_config(lib, oracle, name):
         assert 0.38 <= share[0] <= 0.45
 
 
+@pytest.mark.slow
+def test_large_batch_mixtral_shape(lib, oracle):
+    """Four times the benchmark's batch (T = 65536 tokens, 131072 routed rows,
+    about 9 GB of workspace: 2048-row tiles' worth of rows per expert, 64
+    dispatch chunks) through the default path: routing and dispatch on every
+    token, the output on a seeded sample of tokens."""
+    c = CONFIGS["mixtral"]
+    run_case(lib, oracle, 65536, c.H, c.F, c.E, c.k, seed=c.seed + 1, sample=48)
+
+
 @pytest.mark.parametrize("shape", [(1500, 512, 1408, 8, 2, 0), (2100, 448, 320, 4, 2, 640),
                                    (300, 256, 192, 64, 6, 0)])
 def test_layer_in_cuda_graph(lib, shape):
