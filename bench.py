@@ -149,6 +149,8 @@ def roofline_stage_bytes(cfg):
         "route": T * H * 2 + H * E * 2 + T * k * 8,
         "combine": n_slots * T * H * 4 + T * H * 2,
         "permute_index": R * 4 * 4 + E * 8,
+        # the dispatch with x_perm materialised: the routed rows read and written
+        "permute": 2 * R * H * 2,
     }
 
 
@@ -334,6 +336,10 @@ def bench_ours(args, cfg):
     if not fused_gemms:
         stage_roofline["gemm1"]["frac"] = round(stage_roofline["gemm1"]["tflops"] / peak, 4)
     stage_roofline["route"]["frac"] = round(stage_roofline["route"]["gbs"] / peaks["hbm_gbs"], 4)
+    if plan.x_perm_copy == lib.X_PERM_COPY_KERNEL:
+        # index phases + the x_perm copy, against the copy's algorithmic bytes
+        gbs = by["permute"] / (np.mean(stage_ms["permute"]) * 1e-3) / 1e9
+        stage_roofline["permute"] = {"gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
 
     value = world * flops / (ms * 1e-3) / 1e12
     fused = plan.combine == lib.COMBINE_FUSED
@@ -346,6 +352,8 @@ def bench_ours(args, cfg):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(ms, 4),
+        "step_ms_stats": {"median": round(float(np.median(step_ms)), 4), "min": round(float(np.min(step_ms)), 4),
+                          "max": round(float(np.max(step_ms)), 4)},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
