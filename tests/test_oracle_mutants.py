@@ -42,6 +42,25 @@ MUTANTS = {
                             "for (int32_t n = 0; n < H; ++n) o[n] += y[n];"),
     "x_row_stride": ("const uint16_t* xrow = x + t * (int64_t)H;\n                double* y",
                      "const uint16_t* xrow = x + (t / k) * (int64_t)H;\n                double* y"),
+    # the canonical order: elements of a chunk taken from the top down
+    "chunk_order_reversed": ("for (int32_t h = 8 * c; h < 8 * c + 8 && h < H; ++h) {",
+                             "for (int32_t h = (8 * c + 7 < H ? 8 * c + 7 : H - 1); h >= 8 * c; --h) {"),
+    # the canonical order: 16-element chunks
+    "chunk_of_16": ("int32_t n_chunks = (H + 7) / 8;\n    for (int32_t c = 0; c < n_chunks; ++c) {\n"
+                    "        int L = c % 32;\n        for (int32_t h = 8 * c; h < 8 * c + 8 && h < H; ++h) {",
+                    "int32_t n_chunks = (H + 15) / 16;\n    for (int32_t c = 0; c < n_chunks; ++c) {\n"
+                    "        int L = c % 32;\n        for (int32_t h = 16 * c; h < 16 * c + 16 && h < H; ++h) {"),
+    # the butterfly updated in place, from the top lane down: lane 0 reads a
+    # partner it already overwrote (upwards in place happens to leave lane 0 right)
+    "butterfly_in_place": ("for (int i = 0; i < 32; ++i) next[i] = lane[i] + lane[i ^ s];\n"
+                           "        for (int i = 0; i < 32; ++i) lane[i] = next[i];",
+                           "for (int i = 31; i >= 0; --i) lane[i] = lane[i] + lane[i ^ s];\n"
+                           "        for (int i = 0; i < 32; ++i) next[i] = lane[i];"),
+    # top-k that does not exclude the experts already chosen
+    "topk_no_exclusion": ("                if (taken[e]) continue;\n", "                if (0) continue;\n"),
+    # h rounded to bf16 in the reference (the definition keeps g in full precision)
+    "g_rounded_bf16": ("for (int32_t f = 0; f < F; ++f) g[f] = a[f] / (1.0 + exp(-a[f])) * b[f];",
+                       "for (int32_t f = 0; f < F; ++f) g[f] = (double)(float)(a[f] / (1.0 + exp(-a[f])) * b[f]);"),
 }
 
 
