@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "kernels.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -21,6 +22,8 @@ constexpr int kCombineThreads = 256;
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const float* __restrict__ slot, int n_slots, uint16_t* __restrict__ out, int64_t TH)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const int64_t n_vec = TH / 8;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n_vec; v += stride) {
@@ -58,9 +61,7 @@ cudaError_t launch_combine(const float* slot, int32_t n_slots, uint16_t* out, in
     int64_t blocks = (n_vec + kCombineThreads - 1) / kCombineThreads;
     const int64_t cap = (int64_t)num_sms * 8;   // 8 resident blocks of 256 per SM
     if (blocks > cap) blocks = cap;
-    combine_kernel<<<(int)blocks, kCombineThreads, 0, s>>>(slot, n_slots, out, TH);
-    count_launch();
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel, dim3((unsigned)blocks), dim3(kCombineThreads), 0, s, slot, n_slots, out, TH);
 }
 
 }  // namespace moe

@@ -214,6 +214,24 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         st->abort = 0;
         fence_barrier_init();
     }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB0);
+        if (HAS_GEMM0) tma_prefetch_desc(&tmB1);
+        if (FUSED) {
+            tma_prefetch_desc(&tmA1);
+            tma_prefetch_desc(&tmB2);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc<CG>(smem_u32(&st->tmem_base), TMEM_COLS);
+        tmem_relinquish<CG>();
+    }
+    // launched with programmatic stream serialization: the set-up above is
+    // on-chip only; the tile table and every operand are read after the
+    // kernel before this one has completed
+    pdl_wait();
+    pdl_launch_dependents();
     if (PAIR) {
         // the table of 256-row tiles, from the group offsets (warp 0: a scan)
         if (warp == 0) {
@@ -266,19 +284,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             st->tile_start[i] = st->tile128[i] = args.tile_start[i];
             st->offsets[i] = args.offsets[i];
         }
-    }
-    if (warp == 0 && lane == 0) {
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB0);
-        if (HAS_GEMM0) tma_prefetch_desc(&tmB1);
-        if (FUSED) {
-            tma_prefetch_desc(&tmA1);
-            tma_prefetch_desc(&tmB2);
-        }
-    }
-    if (warp == 1) {
-        tmem_alloc<CG>(smem_u32(&st->tmem_base), TMEM_COLS);
-        tmem_relinquish<CG>();
     }
     tc_fence_before();
     // a pair: both CTAs' barriers are initialised before either signals the other's
@@ -837,11 +842,13 @@ cudaError_t launch_pair(int slot, GemmKernel kern, const CUtensorMap& tmA, const
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)smem_bytes<true>());
     if (err != cudaSuccess) return err;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(NUM_THREADS);
     cfg.dynamicSmemBytes = smem_bytes<true>();
@@ -863,6 +870,7 @@ cudaError_t launch_pair(int slot, GemmKernel kern, const CUtensorMap& tmA, const
     clusters = clusters < num_sms / 2 ? clusters : num_sms / 2;
     if (clusters <= 0) return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3((unsigned)(2 * clusters));
+    cfg.numAttrs = 2;   // the cached occupancy query above saw the cluster shape only
     err = cudaLaunchKernelEx(&cfg, kern, tmA, tmB0, tmB1, tmB0, tmB0, a, a);
     if (err == cudaSuccess) count_launch();
     return err;
@@ -895,9 +903,7 @@ cudaError_t launch_grouped_gemm_fused(int mode, const CUtensorMap& tmA, const CU
     constexpr size_t smem = smem_bytes<false>();
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    kern<<<num_sms, NUM_THREADS, smem, s>>>(tmA, tmB0, tmB1, tmA1, tmB2, a0, a1);
-    count_launch();
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(num_sms), dim3(NUM_THREADS), smem, s, tmA, tmB0, tmB1, tmA1, tmB2, a0, a1);
 }
 
 cudaError_t launch_grouped_gemm(int mode, const CUtensorMap& tmA, const CUtensorMap& tmB0,

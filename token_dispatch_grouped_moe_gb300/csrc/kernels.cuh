@@ -133,6 +133,28 @@ cudaError_t launch_grouped_gemm_fused(int mode, const CUtensorMap& tmA, const CU
 // Counts one kernel launch issued by this library (read with moe_launch_count).
 void count_launch();
 
+// Launches kern<<<grid, block, smem, s>>>(args...) with programmatic stream
+// serialization (the kernel may start before the previous kernel in the stream
+// ends; it calls pdl_wait() before touching global memory) and counts it.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args)
+{
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    if (e == cudaSuccess) count_launch();
+    return e;
+}
+
 cudaError_t launch_combine(const float* slot, int32_t n_slots, uint16_t* out, int64_t T, int32_t H,
                            int num_sms, cudaStream_t s);
 

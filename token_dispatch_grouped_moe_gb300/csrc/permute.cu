@@ -53,7 +53,12 @@ __device__ __forceinline__ void hist_body(const PermuteArgs& a)
         a.hist[(int64_t)blockIdx.x * a.E + e] = hist_s[e];
 }
 
-__global__ void __launch_bounds__(kHistThreads) perm_hist_kernel(PermuteArgs a) { hist_body(a); }
+__global__ void __launch_bounds__(kHistThreads) perm_hist_kernel(PermuteArgs a)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    hist_body(a);
+}
 
 // Exclusive scan of vals[0..n) in place by warp 0 (n <= 256); returns total.
 __device__ int warp0_exclusive_scan(int* vals, int n)
@@ -183,6 +188,8 @@ __device__ __forceinline__ void scatter_body(const PermuteArgs& a, int n_chunks)
 
 __global__ void __launch_bounds__(kScatterThreads) perm_scatter_kernel(PermuteArgs a, int n_chunks)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     scatter_body(a, n_chunks);
 }
 
@@ -190,6 +197,7 @@ __global__ void __launch_bounds__(kScatterThreads) perm_scatter_kernel(PermuteAr
 // barrier between them completes.
 __global__ void __launch_bounds__(kScatterThreads) perm_fused_kernel(PermuteArgs a, int n_chunks)
 {
+    pdl_launch_dependents();   // (a cooperative launch: it starts after the kernel before it)
     hist_body(a);
     __threadfence();
     cooperative_groups::this_grid().sync();
@@ -204,6 +212,8 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t
                                    const int32_t* __restrict__ r_valid, uint16_t* __restrict__ x_perm,
                                    int64_t R, int64_t T, int32_t H, int32_t k, uint32_t* err)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int vec_per_row = H / 8;
@@ -224,6 +234,8 @@ __global__ void tile_table_kernel(const int32_t* __restrict__ offsets, int32_t G
                                   int32_t* __restrict__ tile_start)
 {
     __shared__ int tiles_s[kMaxE];
+    pdl_wait();
+    pdl_launch_dependents();
     for (int g = threadIdx.x; g < G; g += blockDim.x)
         tiles_s[g] = (offsets[g + 1] - offsets[g] + kTileM - 1) / kTileM;
     __syncthreads();
@@ -241,9 +253,7 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s)
     const int n = permute_num_chunks(a.R);
     if (n == 0) {
         // no assignments: zero counts/offsets/tile table via one tiny block
-        perm_scatter_kernel<<<1, kScatterThreads, 0, s>>>(a, 0);
-        count_launch();
-        return cudaGetLastError();
+        return launch_pdl(perm_scatter_kernel, dim3(1), dim3(kScatterThreads), 0, s, a, 0);
     }
     // one cooperative launch while every chunk's block can be resident at once
     int dev = 0, sms = 0, per_sm = 0;
@@ -260,13 +270,9 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s)
         if (e == cudaSuccess) count_launch();
         return e;
     }
-    perm_hist_kernel<<<n, kHistThreads, 0, s>>>(a);
-    count_launch();
-    cudaError_t err = cudaGetLastError();
+    const cudaError_t err = launch_pdl(perm_hist_kernel, dim3(n), dim3(kHistThreads), 0, s, a);
     if (err != cudaSuccess) return err;
-    perm_scatter_kernel<<<n, kScatterThreads, 0, s>>>(a, n);
-    count_launch();
-    return cudaGetLastError();
+    return launch_pdl(perm_scatter_kernel, dim3(n), dim3(kScatterThreads), 0, s, a, n);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* src_row, const int32_t* r_valid,
@@ -276,16 +282,13 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* src_row, const 
     if (R == 0) return cudaSuccess;
     const int64_t blocks_needed = (R + 7) / 8;
     const int grid = (int)(blocks_needed < (int64_t)num_sms * 8 ? blocks_needed : (int64_t)num_sms * 8);
-    gather_rows_kernel<<<grid, 256, 0, s>>>(x, src_row, r_valid, x_perm, R, T, H, k, err);
-    count_launch();
-    return cudaGetLastError();
+    return launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, x, src_row, r_valid, x_perm, R, T, H, k,
+                      err);
 }
 
 cudaError_t launch_tile_table(const int32_t* offsets, int32_t G, int32_t* tile_start, cudaStream_t s)
 {
-    tile_table_kernel<<<1, 256, 0, s>>>(offsets, G, tile_start);
-    count_launch();
-    return cudaGetLastError();
+    return launch_pdl(tile_table_kernel, dim3(1), dim3(256), 0, s, offsets, G, tile_start);
 }
 
 }  // namespace moe

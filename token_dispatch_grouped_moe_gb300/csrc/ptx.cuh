@@ -82,6 +82,25 @@ __device__ __forceinline__ void sleep_ns(unsigned long long ns)
     while (globaltimer_ns() - t0 < ns) __nanosleep(1000);
 }
 
+// ------------------------------------------- programmatic dependent launch --
+
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is still running. pdl_wait() blocks the
+// calling thread until that grid has completed and its memory operations are
+// visible; every thread calls it before its first global memory access. (A
+// no-op for a kernel launched without the attribute.)
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel in the stream be scheduled before this one exits (it
+// still waits in its own pdl_wait() for this grid to complete).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)

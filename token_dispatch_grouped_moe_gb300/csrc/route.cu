@@ -102,6 +102,8 @@ template <int EB, int NT>
 __global__ void __launch_bounds__(kRouteThreads, 1) route_kernel(RouteArgs a, int ms_per_slice)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int Q = EB / 8;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -266,9 +268,7 @@ cudaError_t launch_route_t(const RouteArgs& a, int num_sms, cudaStream_t s)
     if (err != cudaSuccess) return err;
     const int64_t groups = (a.T + (int64_t)kRouteWarps * NT - 1) / ((int64_t)kRouteWarps * NT);
     const int grid = (int)(groups < num_sms ? groups : num_sms);
-    kern<<<grid, kRouteThreads, smem, s>>>(a, ms);
-    count_launch();
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kRouteThreads), smem, s, a, ms);
 }
 
 // ------------------------------------------------------ cluster router --
@@ -434,6 +434,8 @@ template <class S>
 __global__ void __launch_bounds__(kCThreads, S::MINB) route_cluster_kernel(RouteArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
+    pdl_wait();
+    pdl_launch_dependents();
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = S::CS > 1 ? (int)cluster.block_rank() : 0;
     const int warp = threadIdx.x >> 5;
@@ -662,13 +664,15 @@ cudaError_t launch_cluster(const RouteArgs& a, int num_sms, cudaStream_t s)
     cfg.blockDim = dim3(kCThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = S::CS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 1;   // the occupancy query sees the cluster shape only
     int64_t clusters = (int64_t)num_sms * S::MINB / S::CS;
     cfg.gridDim = dim3((unsigned)(clusters * S::CS));
     int max_clusters = 0;
@@ -677,6 +681,7 @@ cudaError_t launch_cluster(const RouteArgs& a, int num_sms, cudaStream_t s)
     if (clusters > groups) clusters = groups;
     if (clusters < 1) clusters = 1;
     cfg.gridDim = dim3((unsigned)(clusters * S::CS));
+    cfg.numAttrs = 2;
     err = cudaLaunchKernelEx(&cfg, kern, a);
     if (err != cudaSuccess) return err;
     count_launch();
@@ -782,6 +787,8 @@ __global__ void __launch_bounds__(S::THREADS, 1)
                         RouteArgs a, int gate_tma, int n_sl)
 {
     extern __shared__ __align__(16) unsigned char smem_raw[];
+    pdl_wait();
+    pdl_launch_dependents();
     constexpr int NT = S::NT, D = S::D, NW = S::NW;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1011,6 +1018,8 @@ __global__ void __launch_bounds__(S::THREADS, 1)
 template <int PMAX>
 __global__ void route_topk_kernel(RouteArgs a)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int r = lane & 7;
     const int E = a.E, k = a.k;
@@ -1105,21 +1114,18 @@ bool launch_stream(const RouteArgs& a, int num_sms, cudaStream_t s, cudaError_t&
     int64_t n_streams = num_sms / n_sl;
     if (n_streams > G) n_streams = G;
     if (n_streams < 1) n_streams = 1;
-    kern<<<(unsigned)(n_streams * n_sl), S::THREADS, smem, s>>>(gmap, xmap, a, gate_tma ? 1 : 0, n_sl);
-    count_launch();
-    err = cudaGetLastError();
+    err = launch_pdl(kern, dim3((unsigned)(n_streams * n_sl)), dim3(S::THREADS), smem, s, gmap, xmap, a,
+                     gate_tma ? 1 : 0, n_sl);
     if (err != cudaSuccess || n_sl == 1) return true;
-    const unsigned blocks = (unsigned)((a.T + 31) / 32);   // 8 warps x 4 tokens
+    const dim3 blocks((unsigned)((a.T + 31) / 32));   // 8 warps x 4 tokens
     if (n_sl <= 4)
-        route_topk_kernel<4><<<blocks, 256, 0, s>>>(a);
+        err = launch_pdl(route_topk_kernel<4>, blocks, dim3(256), 0, s, a);
     else if (n_sl <= 8)
-        route_topk_kernel<8><<<blocks, 256, 0, s>>>(a);
+        err = launch_pdl(route_topk_kernel<8>, blocks, dim3(256), 0, s, a);
     else if (n_sl <= 16)
-        route_topk_kernel<16><<<blocks, 256, 0, s>>>(a);
+        err = launch_pdl(route_topk_kernel<16>, blocks, dim3(256), 0, s, a);
     else
-        route_topk_kernel<32><<<blocks, 256, 0, s>>>(a);
-    count_launch();
-    err = cudaGetLastError();
+        err = launch_pdl(route_topk_kernel<32>, blocks, dim3(256), 0, s, a);
     return true;
 }
 
@@ -1183,6 +1189,8 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s)
 __global__ void shared_gate_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wsg,
                                    float* __restrict__ scale, int64_t T, int32_t H)
 {
+    pdl_wait();
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
@@ -1209,9 +1217,8 @@ cudaError_t launch_shared_gate(const uint16_t* x, const uint16_t* wsg, float* sc
     if (T == 0) return cudaSuccess;
     const int64_t blocks_needed = (T + 7) / 8;
     const int64_t cap = (int64_t)num_sms * 8;
-    shared_gate_kernel<<<(int)(blocks_needed < cap ? blocks_needed : cap), 256, 0, s>>>(x, wsg, scale, T, H);
-    count_launch();
-    return cudaGetLastError();
+    return launch_pdl(shared_gate_kernel, dim3((unsigned)(blocks_needed < cap ? blocks_needed : cap)), dim3(256), 0,
+                      s, x, wsg, scale, T, H);
 }
 
 }  // namespace moe
