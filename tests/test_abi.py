@@ -204,7 +204,6 @@ def test_layer_plan_table(L):
 def test_readme_c_example_compiles(L, tmp_path):
     """The C example in the README compiles and links against include/moe.h
     and the library (no GPU: it is not run)."""
-    import re
     import shutil
     import subprocess
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
