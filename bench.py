@@ -1,6 +1,7 @@
 """Benchmark: forward pass of the Mixtral-shaped MoE layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+    python bench.py --stage route|permute [--T T --H H --E E --k K]   (one stage alone)
 
 A step is one whole layer forward (route -> permute -> GEMM0+SwiGLU ->
 GEMM1+scatter -> combine) over one batch of T tokens, through the C ABI
@@ -450,6 +451,68 @@ def bench_reference(args, cfg):
     }
 
 
+
+def bench_stage(args):
+    """One stage through the C ABI at any shape (--T --H --E --k), outside the
+    layer call: `route` (moe_route; T*H*2 + H*E*2 + T*k*8 bytes) or `permute`
+    (moe_permute with x_perm; 2*T*k*H*2 bytes). Before every timed call L2 is
+    emptied of the inputs by writing and then reading a 256 MiB buffer (the
+    read leaves L2 holding clean lines, so the timed call pays no write-back
+    of the flush); each call is timed with CUDA events on the current stream.
+    Prints one JSON line with the median."""
+    import torch
+    from token_dispatch_grouped_moe_gb300 import build as cuda_build
+    from token_dispatch_grouped_moe_gb300 import lib
+    from token_dispatch_grouped_moe_gb300.inputs import make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("--stage needs a GPU")
+    if not os.path.exists(lib.LIB_PATH):
+        cuda_build.build()
+    lib.load()
+    dev = torch.device("cuda")
+    T, H, E, k = args.T, args.H, args.E, args.k
+    inp = make_inputs(T, H, 64, E, seed=0, only=("x", "Wg"))
+    x, Wg = inp["x"].to(dev), inp["Wg"].to(dev)
+    dims = lib.make_dims(T, H, 64, E, k)
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    ws = None
+    if args.stage == "permute":
+        ws = lib.workspace(dims, device=dev)
+        lib.route(dims, x, Wg, topk_idx=idx, topk_w=w)
+
+    def call():
+        if args.stage == "route":
+            lib.route(dims, x, Wg, topk_idx=idx, topk_w=w)
+        else:
+            lib.permute(dims, idx, ws, x=x, want_x_perm=True)
+
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        flush.view(torch.float32).sum()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1) * 1e-3)
+    if ws is not None and lib.check(ws) != lib.MOE_OK:
+        raise RuntimeError("device error in the stage calls")
+    t = float(np.median(times))
+    work = T * H * 2 + H * E * 2 + T * k * 8 if args.stage == "route" else 2 * T * k * H * 2
+    peaks = measured_peaks()
+    gbs = work / t / 1e9
+    return {"stage": args.stage, "config": {"T": T, "H": H, "E": E, "k": k},
+            "us_median": round(t * 1e6, 2), "us_min": round(min(times) * 1e6, 2),
+            "algorithmic_bytes": work, "gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "peak_source": f"{peaks['source']} HBM copy bandwidth (MEASURED_PEAKS.json)",
+            "steps": args.steps, "warmup": args.warmup}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -468,8 +531,17 @@ def main():
                     help="x_perm filled inside GEMM0 while it runs, or by a kernel before it")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--ref-tokens", type=int, default=64, help="oracle tokens per reference step")
+    ap.add_argument("--stage", choices=["route", "permute"], default=None,
+                    help="time one stage alone at the shape --T --H --E --k instead of the layer")
+    ap.add_argument("--T", type=int, default=8192)
+    ap.add_argument("--H", type=int, default=4096)
+    ap.add_argument("--E", type=int, default=8)
+    ap.add_argument("--k", type=int, default=2)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
+    if args.stage:
+        print(json.dumps(bench_stage(args)), flush=True)
+        return
     cfg = CONFIGS[args.config]
     line = bench_reference(args, cfg) if args.impl == "reference" else bench_ours(args, cfg)
     if line is not None:

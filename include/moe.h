@@ -291,12 +291,16 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* c
  * ints) exceeds 261632 ints are rejected with MOE_ERR_UNSUPPORTED before any
  * launch (for example E = 64 allows T*k up to 8,372,224).
  * The first call on a device looks up the array's device address with that
- * device current; make it before any stream capture on the device. All calls
+ * device current; make it before any stream capture on the device. The
+ * address is cached for the life of the device's context: calling
+ * cudaDeviceReset after the first call is not supported. All calls
  * on a device share the array, which keeps the last call's contents (nothing
  * in it needs to start at zero); calls that overlap on the GPU race on it and
  * must be serialised by the caller. No memory is allocated by this call.
- * An expert id outside [0, E) is skipped (offsets[E] then ends below T*k);
- * there is no device error word.
+ * The shape checks are moe_permute's. An expert id outside [0, E) is
+ * skipped (offsets[E] then ends below T*k); there is no device error word.
+ * With MOE_DEBUG=1 the call synchronises and returns MOE_ERR_CUDA if a
+ * launch faulted.
  */
 moe_status moe_permute_static(const moe_dims* dims, const int32_t* topk_idx, int32_t* counts,
                               int32_t* offsets, int32_t* src_row, int32_t* inv_pos,

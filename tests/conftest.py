@@ -8,8 +8,6 @@ TESTS = os.path.dirname(os.path.abspath(__file__))
 for _p in (ROOT, TESTS):
     if _p not in sys.path:
         sys.path.insert(0, _p)
-if False:
-    sys.path.insert(0, ROOT)
 
 
 def pytest_configure(config):

@@ -201,24 +201,20 @@ def test_layer_plan_table(L):
         lib.layer_plan(lib.make_dims(64, 100, 64, 8, 2))   # H not a multiple of 64
 
 
-def test_readme_c_example_compiles(L, tmp_path):
-    """The C example in the README compiles and links against include/moe.h
-    and the library (no GPU: it is not run)."""
+def test_c_example_compiles(L, tmp_path):
+    """include/example.c (one layer call in C) compiles and links against
+    include/moe.h and the library (no GPU: it is not run)."""
     import shutil
     import subprocess
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    text = open(os.path.join(root, "README.md")).read()
-    m = re.search(r"```c\n(.*?)```", text, re.S)
-    assert m, "no C example in the README"
-    src = tmp_path / "example.c"
-    src.write_text(m.group(1) + "\nint main(void) { return 0; }\n")
+    src = os.path.join(root, "include", "example.c")
     cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
     gcc = shutil.which("gcc")
     if gcc is None or not os.path.exists(os.path.join(cuda, "include", "cuda_runtime.h")):
         pytest.skip("no C compiler or CUDA headers")
     pkg = os.path.join(root, "token_dispatch_grouped_moe_gb300")
-    cmd = [gcc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(root, "include"), "-I",
-           os.path.join(cuda, "include"), str(src), "-o", str(tmp_path / "example"), "-L", pkg,
+    cmd = [gcc, "-std=c11", "-Wall", "-Werror", "-DMOE_EXAMPLE_MAIN", "-I", os.path.join(root, "include"),
+           "-I", os.path.join(cuda, "include"), src, "-o", str(tmp_path / "example"), "-L", pkg,
            "-lmoe_gb300", "-L", os.path.join(cuda, "lib64"), "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     assert r.returncode == 0, r.stderr

@@ -15,6 +15,8 @@ import torch
 from token_dispatch_grouped_moe_gb300.configs import CONFIGS
 from token_dispatch_grouped_moe_gb300.inputs import bf16_bits, bits_to_bf16, make_inputs
 
+from sampling import tile_coverage, tile_stratified_tokens
+
 pytestmark = pytest.mark.gpu
 
 TOL_OUT = 2e-2       # max |out - ref| / rms(ref)
@@ -112,18 +114,24 @@ def run_case(lib, oracle, T, H, F, E, k, Fs=0, seed=0, bias=None, sample=None, c
     assert np.array_equal(routing.topk_idx.cpu().numpy(), idx), "top-k ids differ"
     gw = routing.topk_w.cpu().numpy()
     assert np.allclose(gw, w, rtol=TOL_W, atol=1e-7), f"gate weights differ: {np.max(np.abs(gw - w))}"
+    counts, offsets, src_row, inv_pos = oracle.permute(idx, E)
     if check_perm:
-        counts, offsets, src_row, inv_pos = oracle.permute(idx, E)
         assert np.array_equal(routing.counts.cpu().numpy(), counts)
         assert np.array_equal(routing.offsets.cpu().numpy(), offsets)
         assert np.array_equal(routing.src_row.cpu().numpy(), src_row)
         assert np.array_equal(routing.inv_pos.cpu().numpy(), inv_pos)
-    # output rows: all tokens, or a seeded sample at large sizes
+    # output rows: all tokens, or at large sizes a sample that reaches every
+    # GEMM tile (tile_stratified_tokens) plus seeded random tokens
     if sample is None or sample >= T:
         tokens = np.arange(T, dtype=np.int64)
     else:
         rng = np.random.default_rng(seed + 99)
-        tokens = np.unique(np.concatenate([[0, T - 1], rng.choice(T, sample, replace=False)]))
+        strat = tile_stratified_tokens(offsets, src_row, k, T, Fs)
+        tokens = np.unique(np.concatenate([strat, [0, T - 1], rng.choice(T, sample, replace=False)]))
+        covered, n_tiles = tile_coverage(tokens, inv_pos, offsets, k, T, Fs)
+        assert covered == n_tiles, f"sample reaches {covered} of {n_tiles} row tiles"
+        print(f"[{T}x{H} F={F} E={E} k={k} Fs={Fs}] compared rows: {tokens.size} tokens; "
+              f"row tiles covered = all ({covered} of {n_tiles})")
     ref = oracle.layer_rows(tokens, idx, w, b["x"], b["W1"], b["W3"], b["W2"], b.get("W1s"),
                             b.get("W3s"), b.get("W2s"), shared_scale=scale)
     o = out.float().cpu().numpy()[tokens].astype(np.float64)
@@ -660,8 +668,11 @@ def test_full_qwen2_gating_variants(lib, oracle):
 @pytest.mark.parametrize("name", FULL)
 def test_full_config(lib, oracle, name):
     """The configurations at full size, launched as the benchmark launches
-    them. Routing and dispatch are compared on every token; the output on a
-    seeded sample of tokens (rows are independent, so the sample is exact)."""
+    them. Routing and dispatch are compared on every token; the output on the
+    rows that reach every M tile of both expert GEMMs (first and last row of
+    each 128-row tile of each expert, every tile of the shared expert) plus a
+    seeded random sample (rows are independent, so each compared row is
+    exact)."""
     c = CONFIGS[name]
     bias = zipf_bias() if c.zipf else None
     r = run_case(lib, oracle, c.T, c.H, c.F, c.E, c.k, Fs=c.Fs, seed=c.seed, bias=bias, sample=48)
@@ -675,7 +686,7 @@ def test_large_batch_mixtral_shape(lib, oracle):
     """Four times the benchmark's batch (T = 65536 tokens, 131072 routed rows,
     about 9 GB of workspace: 2048-row tiles' worth of rows per expert, 64
     dispatch chunks) through the default path: routing and dispatch on every
-    token, the output on a seeded sample of tokens."""
+    token, the output on rows reaching every GEMM tile plus a seeded sample."""
     c = CONFIGS["mixtral"]
     run_case(lib, oracle, 65536, c.H, c.F, c.E, c.k, seed=c.seed + 1, sample=48)
 

@@ -41,15 +41,6 @@ int num_sms_current()
     return n;
 }
 
-bool debug_mode()
-{
-    static const bool on = [] {
-        const char* v = std::getenv("MOE_DEBUG");
-        return v && v[0] && std::strcmp(v, "0") != 0;
-    }();
-    return on;
-}
-
 // ---------------------------------------------------------- tensor maps --
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -211,20 +202,6 @@ Layout layout_of(const moe_dims& d)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-moe_status check_dims(const moe_dims* d)
-{
-    if (!d) return MOE_ERR_INVALID_ARG;
-    if (d->T < 0 || d->H <= 0 || d->F <= 0 || d->E <= 0 || d->k <= 0 || d->F_shared < 0)
-        return MOE_ERR_INVALID_ARG;
-    if (d->k > d->E) return MOE_ERR_INVALID_ARG;
-    if (d->k > 8 || d->E > 256) return MOE_ERR_UNSUPPORTED;
-    if (d->H % 64 || d->F % 64 || d->F_shared % 64) return MOE_ERR_UNSUPPORTED;
-    if (d->T * (int64_t)d->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
-    if ((int64_t)d->E * d->H >= ((int64_t)1 << 31) || (int64_t)d->E * d->F >= ((int64_t)1 << 31))
-        return MOE_ERR_UNSUPPORTED;
-    return MOE_OK;
-}
-
 moe_status check_ws(const moe_dims& d, void* ws, size_t ws_bytes)
 {
     if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_WORKSPACE;
@@ -365,6 +342,29 @@ void record(moe_event_t ev, cudaStream_t s)
 }  // namespace
 
 void count_launch() { g_launch_count.fetch_add(1, std::memory_order_relaxed); }
+
+bool debug_mode()
+{
+    static const bool on = [] {
+        const char* v = std::getenv("MOE_DEBUG");
+        return v && v[0] && std::strcmp(v, "0") != 0;
+    }();
+    return on;
+}
+
+moe_status check_dims(const moe_dims* d)
+{
+    if (!d) return MOE_ERR_INVALID_ARG;
+    if (d->T < 0 || d->H <= 0 || d->F <= 0 || d->E <= 0 || d->k <= 0 || d->F_shared < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (d->k > d->E) return MOE_ERR_INVALID_ARG;
+    if (d->k > 8 || d->E > 256) return MOE_ERR_UNSUPPORTED;
+    if (d->H % 64 || d->F % 64 || d->F_shared % 64) return MOE_ERR_UNSUPPORTED;
+    if (d->T * (int64_t)d->k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    if ((int64_t)d->E * d->H >= ((int64_t)1 << 31) || (int64_t)d->E * d->F >= ((int64_t)1 << 31))
+        return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+}
 
 }  // namespace moe
 

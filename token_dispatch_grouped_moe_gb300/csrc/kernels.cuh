@@ -8,7 +8,15 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "../../include/moe.h"
+
 namespace moe {
+
+// The host checks of a moe_dims that every entry point shares (null, signs,
+// k <= E, the supported sizes); MOE_OK or the status to return.
+moe_status check_dims(const moe_dims* d);
+// MOE_DEBUG=1 (read once): every entry point synchronises and checks.
+bool debug_mode();
 
 constexpr int kTileM = 128;   // GEMM M tile (routed rows per tile)
 // GEMM K per pipeline stage: 64 bf16 (128-byte A rows, 128-byte swizzle, 4

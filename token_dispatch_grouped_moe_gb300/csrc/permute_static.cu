@@ -13,7 +13,12 @@
 // Rules of this entry point:
 //   - The first call on a device looks up the device address of the array
 //     (cudaGetSymbolAddress, with that device current) and caches it; make
-//     that first call before any stream capture on the device.
+//     that first call before any stream capture on the device. The cached
+//     address lives as long as the device's context: a cudaDeviceReset after
+//     the first call is not supported (the module is loaded afresh and the
+//     array may move).
+//   - The same shape rules as moe_permute (check_dims), and with MOE_DEBUG=1
+//     the call synchronises and reports a launch fault as MOE_ERR_CUDA.
 //   - All calls on a device share the one array and it keeps the contents of
 //     the last call. Nothing in it has to start at zero: every call writes
 //     the part it reads. Calls that overlap on the GPU (other streams, other
@@ -87,11 +92,10 @@ extern "C" moe_status moe_permute_static(const moe_dims* dims, const int32_t* to
                                          int32_t* inv_pos, const moe_bf16* x, moe_bf16* x_perm,
                                          moe_stream_t stream)
 {
-    if (!dims) return MOE_ERR_INVALID_ARG;
+    // the same shape rules as moe_permute, then the array's limit
+    const moe_status dims_ok = moe::check_dims(dims);
+    if (dims_ok != MOE_OK) return dims_ok;
     const moe_dims& d = *dims;
-    if (d.T < 0 || d.H <= 0 || d.E <= 0 || d.k <= 0 || d.k > d.E) return MOE_ERR_INVALID_ARG;
-    if (d.k > 8 || d.E > 256 || d.H % 64) return MOE_ERR_UNSUPPORTED;
-    if (d.T * (int64_t)d.k >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
     const int64_t R = d.T * d.k;
     const int64_t hist_ints = (int64_t)moe::permute_num_chunks(R) * d.E;
     if (hist_ints > kStaticScratchInts - kTileTableInts) return MOE_ERR_UNSUPPORTED;
@@ -113,5 +117,10 @@ extern "C" moe_status moe_permute_static(const moe_dims* dims, const int32_t* to
     if (x_perm && moe::launch_gather_rows(x, src_row, offsets + d.E, x_perm, R, d.T, d.H, d.k, nullptr,
                                           sms, s) != cudaSuccess)
         return MOE_ERR_CUDA;
+    if (moe::debug_mode()) {
+        // MOE_DEBUG=1: wait for the launches and report a fault they raised
+        if (cudaStreamSynchronize(s) != cudaSuccess || cudaGetLastError() != cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
     return MOE_OK;
 }
