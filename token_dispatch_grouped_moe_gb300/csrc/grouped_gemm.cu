@@ -786,36 +786,67 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
                 // the warp sums its finished rows together: lane l takes columns
-                // 8l .. 8l+7, so each slot row is read as one coalesced 1 KB line
+                // 8l .. 8l+7, so each slot row is read as one coalesced 1 KB line;
+                // CB rows at a time, their loads issued together so that the
+                // L2 round trips of CB rows overlap
                 unsigned todo = __ballot_sync(0xffffffffu, last);
                 if (todo) __threadfence();
                 const int n0 = wk.n_tile * BN;
                 const int c = 8 * lane;
                 const int64_t TN = args.T * (int64_t)N1;
+                constexpr int CB = 4;
                 while (todo) {
-                    const int src_lane = __ffs(todo) - 1;
-                    todo &= todo - 1;
-                    const int64_t tt = __shfl_sync(0xffffffffu, t, src_lane);
-                    if (n0 + c < N1) {
-                        const float* src = slot + tt * N1 + n0 + c;
-                        float4 a0 = __ldcg(reinterpret_cast<const float4*>(src));
-                        float4 a1 = __ldcg(reinterpret_cast<const float4*>(src + 4));
-                        for (int jj = 1; jj < n_slots; ++jj) {
-                            const float4 b0 = __ldcg(reinterpret_cast<const float4*>(src + jj * TN));
-                            const float4 b1 = __ldcg(reinterpret_cast<const float4*>(src + jj * TN + 4));
-                            a0.x = a0.x + b0.x; a0.y = a0.y + b0.y; a0.z = a0.z + b0.z; a0.w = a0.w + b0.w;
-                            a1.x = a1.x + b1.x; a1.y = a1.y + b1.y; a1.z = a1.z + b1.z; a1.w = a1.w + b1.w;
+                    int64_t tt[CB];
+#pragma unroll
+                    for (int u = 0; u < CB; ++u) {
+                        tt[u] = -1;
+                        if (todo) {   // warp-uniform: todo is a ballot
+                            const int src_lane = __ffs(todo) - 1;
+                            todo &= todo - 1;
+                            tt[u] = __shfl_sync(0xffffffffu, t, src_lane);
                         }
-                        __nv_bfloat162 p0 = __floats2bfloat162_rn(a0.x, a0.y);
-                        __nv_bfloat162 p1 = __floats2bfloat162_rn(a0.z, a0.w);
-                        __nv_bfloat162 p2 = __floats2bfloat162_rn(a1.x, a1.y);
-                        __nv_bfloat162 p3 = __floats2bfloat162_rn(a1.z, a1.w);
-                        uint4 o;
-                        o.x = *reinterpret_cast<uint32_t*>(&p0);
-                        o.y = *reinterpret_cast<uint32_t*>(&p1);
-                        o.z = *reinterpret_cast<uint32_t*>(&p2);
-                        o.w = *reinterpret_cast<uint32_t*>(&p3);
-                        *reinterpret_cast<uint4*>(out + tt * N1 + n0 + c) = o;
+                    }
+                    if (n0 + c < N1) {
+                        float4 a0[CB], a1[CB];
+#pragma unroll
+                        for (int u = 0; u < CB; ++u) {
+                            if (tt[u] < 0) continue;
+                            const float* src = slot + tt[u] * N1 + n0 + c;
+                            a0[u] = __ldcg(reinterpret_cast<const float4*>(src));
+                            a1[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+                        }
+                        for (int jj = 1; jj < n_slots; ++jj) {
+                            float4 b0[CB], b1[CB];
+#pragma unroll
+                            for (int u = 0; u < CB; ++u) {
+                                if (tt[u] < 0) continue;
+                                const float* src = slot + tt[u] * N1 + n0 + c + jj * TN;
+                                b0[u] = __ldcg(reinterpret_cast<const float4*>(src));
+                                b1[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+                            }
+#pragma unroll
+                            for (int u = 0; u < CB; ++u) {
+                                if (tt[u] < 0) continue;
+                                a0[u].x = a0[u].x + b0[u].x; a0[u].y = a0[u].y + b0[u].y;
+                                a0[u].z = a0[u].z + b0[u].z; a0[u].w = a0[u].w + b0[u].w;
+                                a1[u].x = a1[u].x + b1[u].x; a1[u].y = a1[u].y + b1[u].y;
+                                a1[u].z = a1[u].z + b1[u].z; a1[u].w = a1[u].w + b1[u].w;
+                            }
+                        }
+#pragma unroll
+                        for (int u = 0; u < CB; ++u) {
+                            if (tt[u] < 0) continue;
+                            __nv_bfloat162 p0 = __floats2bfloat162_rn(a0[u].x, a0[u].y);
+                            __nv_bfloat162 p1 = __floats2bfloat162_rn(a0[u].z, a0[u].w);
+                            __nv_bfloat162 p2 = __floats2bfloat162_rn(a1[u].x, a1[u].y);
+                            __nv_bfloat162 p3 = __floats2bfloat162_rn(a1[u].z, a1[u].w);
+                            uint4 o;
+                            o.x = *reinterpret_cast<uint32_t*>(&p0);
+                            o.y = *reinterpret_cast<uint32_t*>(&p1);
+                            o.z = *reinterpret_cast<uint32_t*>(&p2);
+                            o.w = *reinterpret_cast<uint32_t*>(&p3);
+                            *reinterpret_cast<uint4*>(out + tt[u] * N1 + n0 + c) = o;
+                        }
                     }
                 }
             }
