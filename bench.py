@@ -209,6 +209,8 @@ def bench_ours(args, cfg):
                        "pair": lib.CTA_GROUP_PAIR}[args.cta_group])
     lib.set_x_perm_copy({"auto": lib.X_PERM_COPY_AUTO, "inline": lib.X_PERM_COPY_INLINE,
                          "kernel": lib.X_PERM_COPY_KERNEL}[args.x_perm_copy])
+    lib.set_router({"auto": lib.ROUTER_OPT_AUTO, "fma": lib.ROUTER_OPT_FMA,
+                    "tensor": lib.ROUTER_OPT_TENSOR}[args.router])
 
     inp, g = make_workload(cfg, device)
     dims = lib.make_dims(cfg.T, cfg.H, cfg.F, cfg.E, cfg.k, cfg.Fs)
@@ -379,6 +381,7 @@ def bench_ours(args, cfg):
         "timing": {"value": "K layer calls, one event pair each, no events between stages",
                    "stage_ms": "a second pass of K calls with an event before every stage",
                    "stage_pass_ms_per_step": round(stage_step_ms, 4)},
+        "router": {0: "stream", 1: "sliced", 2: "cluster", 3: "block", 4: "tensor"}.get(plan.router),
         "gemm_plan": {"cta_group": plan.cta_group, "cta_group_gemm1": plan.cta_group_gemm1,
                       "tile": [plan.tile_m, plan.tile_n, plan.tile_k],
                       "stages": plan.stages, "one_launch": fused_gemms, "combine_fused": fused,
@@ -529,6 +532,8 @@ def main():
                     help="CTAs per tensor-core MMA in the dense-A expert GEMMs")
     ap.add_argument("--x-perm-copy", default="auto", choices=["auto", "inline", "kernel"],
                     help="x_perm filled inside GEMM0 while it runs, or by a kernel before it")
+    ap.add_argument("--router", default="auto", choices=["auto", "fma", "tensor"],
+                    help="the router kernels: the table's choice, the FMA routers, or the tensor-core router")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--ref-tokens", type=int, default=64, help="oracle tokens per reference step")
     ap.add_argument("--stage", choices=["route", "permute"], default=None,

@@ -174,7 +174,23 @@ enum {
     MOE_OPT_X_PERM_COPY = 4,
     MOE_X_PERM_COPY_AUTO = 0,
     MOE_X_PERM_COPY_INLINE = 1,
-    MOE_X_PERM_COPY_KERNEL = 2
+    MOE_X_PERM_COPY_KERNEL = 2,
+    /* Which router moe_layer_forward runs:
+     *   MOE_ROUTER_OPT_AUTO   (default) the table (see moe_layer_plan): the
+     *                         tensor-core router for 16 <= E <= 64 (E a
+     *                         multiple of 8) from T = 8192, where it measured
+     *                         faster, else an FMA router;
+     *   MOE_ROUTER_OPT_FMA    the FMA routers (the canonical order itself);
+     *   MOE_ROUTER_OPT_TENSOR the tensor-core router wherever it applies
+     *                         (8 <= E <= 64, E a multiple of 8, T >= 512).
+     * The expert ids and their order are the same bit for bit either way
+     * (the tensor-core router proves each token's selection against the
+     * canonical order, or recomputes the token in it); the gate weights agree
+     * to fp32 rounding (a softmax of logits whose summation order differs). */
+    MOE_OPT_ROUTER = 5,
+    MOE_ROUTER_OPT_AUTO = 0,
+    MOE_ROUTER_OPT_FMA = 1,
+    MOE_ROUTER_OPT_TENSOR = 2
 };
 
 /* Sets a library-wide option for later calls (all devices and threads).
@@ -185,13 +201,18 @@ moe_status moe_set_option(int option, int value);
 /* Current value of an option, or -1 for an unknown option. */
 int moe_get_option(int option);
 
-/* Router kernels (moe_plan.router). All compute the same logits bit for bit. */
+/* Router kernels (moe_plan.router). All select the same experts in the same
+ * order bit for bit; the FMA routers (0..3) also give the same logits. */
 enum {
     MOE_ROUTER_STREAM = 0,   /* E <= 8: TMA-fed per-warp pipelines, top-k fused */
     MOE_ROUTER_SLICED = 1,   /* E > 8, a multiple of 8, inside moe_layer_forward: expert
                               * slices of 8 per CTA, logits to the workspace, top-k pass */
     MOE_ROUTER_CLUSTER = 2,  /* 8 < E <= 64: canonical lanes split over a CTA cluster */
-    MOE_ROUTER_BLOCK = 3     /* anything else: one CTA per SM, gate staged in slices */
+    MOE_ROUTER_BLOCK = 3,    /* anything else: one CTA per SM, gate staged in slices */
+    MOE_ROUTER_TENSOR = 4    /* inside moe_layer_forward, 8 <= E <= 64, E % 8 == 0: the
+                              * gate GEMM on tcgen05; each token's top-k proven equal to
+                              * the canonical order's by an error bound (ties and near
+                              * ties recomputed in the canonical order) */
 };
 
 /* The configuration moe_layer_forward runs for a shape under the current
@@ -224,6 +245,24 @@ moe_status moe_layer_plan(const moe_dims* dims, moe_plan* plan);
  * the wait somehow completed, MOE_ERR_CUDA on a launch or copy error. The
  * device stays usable. Synchronises `stream`. */
 moe_status moe_selftest_wait_timeout(int32_t limit_ms, moe_stream_t stream);
+
+/* Test hook of the tensor-core router (MOE_ROUTER_TENSOR): routes x with it
+ * as moe_layer_forward would, writing topk_idx[T,k] / topk_w[T,k] and
+ * optionally
+ *   fast_logits[T,E]  the tensor-core logits (before the bias),
+ *   fast_bound[T]     the bound used for the tensor-core part of the error,
+ *                     c_fast ||x_t|| max_e ||w_e||, so that a caller can check
+ *                     |fast_logits - exact| <= fast_bound,
+ *   n_exact           how many tokens took the canonical recomputation
+ *                     (reading it synchronises `stream`).
+ * force_exact != 0 sends every token through the canonical recomputation.
+ * ws is a moe_layer_forward workspace for dims. MOE_ERR_UNSUPPORTED where the
+ * tensor-core router does not apply. Not needed for normal use. */
+moe_status moe_selftest_route_tc(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg,
+                                 const float* bias, int32_t renormalize, int32_t force_exact,
+                                 int32_t* topk_idx, float* topk_w, float* fast_logits,
+                                 float* fast_bound, int64_t* n_exact, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream);
 
 /* Library version (major*10000 + minor*100 + patch). */
 int moe_version(void);

@@ -141,8 +141,8 @@ def test_layer_plan_table(L):
         "qwen2": (lib.ROUTER_SLICED, lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF, 1, 2),
         "dsk-1k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON, 1, 1),
         "dsk-4k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON, 1, 1),
-        "dsk-16k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_OFF, 2, 2),
-        "dsk-32k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_OFF, 2, 2),
+        "dsk-16k": (lib.ROUTER_TENSOR, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_OFF, 2, 2),
+        "dsk-32k": (lib.ROUTER_TENSOR, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_OFF, 2, 2),
     }
     for name, (router, combine, fusion, cg, cg1) in want.items():
         c = CONFIGS[name]
@@ -183,6 +183,23 @@ def test_layer_plan_table(L):
     assert lib.layer_plan(lib.make_dims(64, 256, 64, 200, 2)).router == lib.ROUTER_SLICED
     assert lib.layer_plan(lib.make_dims(64, 256, 64, 196, 2)).router == lib.ROUTER_BLOCK
     assert lib.layer_plan(lib.make_dims(64, 16384, 64, 8, 2)).router == lib.ROUTER_BLOCK
+    # the tensor-core router by default for 16 <= E <= 64 (a multiple of 8)
+    # from 8192 tokens; forced by the option from 512 tokens and E >= 8; the
+    # other option value keeps the FMA routers
+    assert lib.layer_plan(lib.make_dims(8192, 256, 64, 64, 6)).router == lib.ROUTER_TENSOR
+    assert lib.layer_plan(lib.make_dims(8191, 256, 64, 64, 6)).router == lib.ROUTER_SLICED
+    assert lib.layer_plan(lib.make_dims(65536, 4096, 64, 8, 2)).router == lib.ROUTER_STREAM
+    assert lib.layer_plan(lib.make_dims(16384, 256, 64, 12, 2)).router == lib.ROUTER_CLUSTER
+    assert lib.layer_plan(lib.make_dims(16384, 256, 64, 72, 2)).router == lib.ROUTER_SLICED
+    try:
+        lib.set_router(lib.ROUTER_OPT_TENSOR)
+        assert lib.layer_plan(lib.make_dims(512, 256, 64, 64, 6)).router == lib.ROUTER_TENSOR
+        assert lib.layer_plan(lib.make_dims(8192, 4096, 64, 8, 2)).router == lib.ROUTER_TENSOR
+        assert lib.layer_plan(lib.make_dims(511, 256, 64, 64, 6)).router == lib.ROUTER_SLICED
+        lib.set_router(lib.ROUTER_OPT_FMA)
+        assert lib.layer_plan(lib.make_dims(32768, 2048, 64, 64, 6)).router == lib.ROUTER_SLICED
+    finally:
+        lib.set_router(lib.ROUTER_OPT_AUTO)
     # options override the automatic entries; a gather A path rules out fusion
     d = lib.make_dims(1024, 2048, 1408, 64, 6)
     try:

@@ -20,7 +20,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libmoe_gb300.so")
-SOURCES = ["route.cu", "permute.cu", "permute_static.cu", "grouped_gemm.cu", "combine.cu", "api.cu",
+SOURCES = ["route.cu", "route_tc.cu", "permute.cu", "permute_static.cu", "grouped_gemm.cu", "combine.cu", "api.cu",
            "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", *ARCH]

@@ -27,6 +27,7 @@ std::atomic<int> g_combine{MOE_COMBINE_AUTO};
 std::atomic<int> g_gemm_fusion{MOE_GEMM_FUSION_AUTO};
 std::atomic<int> g_cta_group{MOE_CTA_GROUP_AUTO};
 std::atomic<int> g_x_perm_copy{MOE_X_PERM_COPY_AUTO};
+std::atomic<int> g_router{MOE_ROUTER_OPT_AUTO};
 std::atomic<unsigned long long> g_launch_count{0};
 
 int num_sms_current()
@@ -137,6 +138,17 @@ moe_plan plan_of(const moe_dims& d)
 {
     moe_plan p{};
     p.router = route_variant(d.H, d.E, /*has_logits=*/true);
+    const int router_opt = g_router.load();
+    // the tensor-core router (the ids are the same either way): forced by the
+    // option wherever it applies, else where it measured faster than the FMA
+    // routers on GB300: E >= 16 from 8192 tokens (DeepSeek-shaped T = 16384:
+    // 107 -> 63 us, T = 32768: 206 -> 104 us). Below that, and for E = 8, the
+    // FMA routers are as fast or faster (Mixtral-shaped 27 vs 52 us, Qwen2-
+    // shaped 64 vs 69 us, DeepSeek-shaped T = 1024 26 vs 43 us).
+    if (route_tc_supported(d.T, d.H, d.E) &&
+        (router_opt == MOE_ROUTER_OPT_TENSOR ||
+         (router_opt == MOE_ROUTER_OPT_AUTO && d.E >= 16 && d.T >= 8192)))
+        p.router = MOE_ROUTER_TENSOR;
     p.gemm0_a = g_gemm0_a.load();
     const int combine_opt = g_combine.load();
     const int32_t k_last = d.F_shared > 0 ? d.F_shared : d.F;
@@ -168,7 +180,8 @@ moe_plan plan_of(const moe_dims& d)
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
-    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, arrive, sgate, logits, ready, total;
+    size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, arrive, sgate, logits, ready;
+    size_t tc_wgt, tc_wnorm, tc_nflag, tc_tok, tc_cand, tc_ftok, tc_fcand, tc_fsel, tc_fselv, total;
 };
 
 Layout layout_of(const moe_dims& d)
@@ -194,6 +207,19 @@ Layout layout_of(const moe_dims& d)
     L.sgate = o; o += al256(T * 4);
     L.logits = o; o += al256(E > 8 ? T * E * 4 : 0);   // the sliced router's logits
     L.ready = o; o += al256(((R + kTileM - 1) / kTileM + E + 1) * 4);   // fused GEMMs: per M tile
+    // the tensor-core router: transposed gate, column norms, the list of
+    // tokens recomputed in the canonical order
+    const bool tc = route_tc_supported((int64_t)T, d.H, d.E) || (d.E >= 8 && d.E <= 64 && d.E % 8 == 0);
+    const size_t np = tc ? (size_t)route_tc_np(d.E) : 0;
+    L.tc_wgt = o; o += al256(np * (size_t)d.H * 2);
+    L.tc_wnorm = o; o += al256(np * (size_t)(d.H / 64) * 4);
+    L.tc_nflag = o; o += al256(tc ? 4 : 0);
+    L.tc_tok = o; o += al256(tc ? T * 4 : 0);                  // per-token bound
+    L.tc_cand = o; o += al256(tc ? T * (size_t)d.E * 4 : 0);   // fast logits
+    L.tc_ftok = o; o += al256(tc ? T * 4 : 0);                  // listed tokens
+    L.tc_fcand = o; o += al256(tc ? T * 8 : 0);
+    L.tc_fsel = o; o += al256(tc ? T * 9 * 4 : 0);
+    L.tc_fselv = o; o += al256(tc ? T * 9 * 4 : 0);
     L.total = o;
     return L;
 }
@@ -248,6 +274,21 @@ struct FusedCombine {
     uint16_t* out;
     int32_t n_tickets = 0;
 };
+
+RouteTcArgs tc_args_of(const Layout& L, unsigned char* w)
+{
+    RouteTcArgs c;
+    c.wgt = reinterpret_cast<uint16_t*>(w + L.tc_wgt);
+    c.wpart = reinterpret_cast<float*>(w + L.tc_wnorm);
+    c.n_exact = reinterpret_cast<int32_t*>(w + L.tc_nflag);
+    c.bound = reinterpret_cast<float*>(w + L.tc_tok);
+    c.fast = reinterpret_cast<float*>(w + L.tc_cand);
+    c.flag_tok = reinterpret_cast<int32_t*>(w + L.tc_ftok);
+    c.flag_cand = reinterpret_cast<uint64_t*>(w + L.tc_fcand);
+    c.flag_sel = reinterpret_cast<int32_t*>(w + L.tc_fsel);
+    c.flag_selv = reinterpret_cast<float*>(w + L.tc_fselv);
+    return c;
+}
 
 moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, int32_t k,
                             const uint16_t* x, const uint16_t* x_rows, const int32_t* src_row,
@@ -423,6 +464,12 @@ moe_status moe_set_option(int option, int value)
         g_x_perm_copy.store(value);
         return MOE_OK;
     }
+    if (option == MOE_OPT_ROUTER) {
+        if (value != MOE_ROUTER_OPT_AUTO && value != MOE_ROUTER_OPT_FMA && value != MOE_ROUTER_OPT_TENSOR)
+            return MOE_ERR_INVALID_ARG;
+        g_router.store(value);
+        return MOE_OK;
+    }
     return MOE_ERR_INVALID_ARG;
 }
 
@@ -433,6 +480,7 @@ int moe_get_option(int option)
     if (option == MOE_OPT_GEMM_FUSION) return g_gemm_fusion.load();
     if (option == MOE_OPT_CTA_GROUP) return g_cta_group.load();
     if (option == MOE_OPT_X_PERM_COPY) return g_x_perm_copy.load();
+    if (option == MOE_OPT_ROUTER) return g_router.load();
     return -1;
 }
 
@@ -641,7 +689,10 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     ra.renorm = gating ? (gating->renormalize != 0) : 1;
     ra.err = err;
     ra.logits = reinterpret_cast<float*>(w + L.logits);
-    MOE_TRY(launch_route(ra, sms, s));
+    if (plan.router == MOE_ROUTER_TENSOR)
+        MOE_TRY(launch_route_tc(ra, tc_args_of(L, w), sms, s));
+    else
+        MOE_TRY(launch_route(ra, sms, s));
 
     record(events ? events->before_permute : nullptr, s);
     PermuteArgs pa{idx, counts, offsets, src, inv, tile, reinterpret_cast<int32_t*>(w + L.hist), err,
@@ -695,6 +746,40 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     if (!fused)   // else GEMM1's epilogue finished it (the last contribution)
         MOE_TRY(launch_combine(slot, n_slots, out, d.T, d.H, sms, s));
     record(events ? events->after_combine : nullptr, s);
+    return finish(cudaSuccess, ws, s);
+}
+
+moe_status moe_selftest_route_tc(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg,
+                                 const float* bias, int32_t renormalize, int32_t force_exact,
+                                 int32_t* topk_idx, float* topk_w, float* fast_logits,
+                                 float* fast_bound, int64_t* n_exact, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream)
+{
+    MOE_TRY_STATUS(check_dims(dims));
+    MOE_TRY_STATUS(check_ws(*dims, ws, ws_bytes));
+    const moe_dims& d = *dims;
+    if (!route_tc_supported(d.T, d.H, d.E)) return MOE_ERR_UNSUPPORTED;
+    if (!x || !Wg || !topk_idx || !topk_w || !aligned16(x) || !aligned16(Wg)) return MOE_ERR_INVALID_ARG;
+    if ((fast_logits == nullptr) != (fast_bound == nullptr)) return MOE_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const Layout L = layout_of(d);
+    unsigned char* w = bytes(ws);
+    RouteArgs ra{x, Wg, bias, topk_idx, topk_w, d.T, d.H, d.E, d.k};
+    ra.renorm = renormalize != 0;
+    ra.err = reinterpret_cast<uint32_t*>(w + L.err);
+    RouteTcArgs c = tc_args_of(L, w);
+    c.force_exact = force_exact != 0;
+    c.dbg_fast = fast_logits;
+    c.dbg_bound = fast_bound;
+    MOE_TRY(launch_route_tc(ra, c, sms, s));
+    if (n_exact) {
+        int32_t n = 0;
+        MOE_TRY(cudaMemcpyAsync(&n, c.n_exact, sizeof n, cudaMemcpyDeviceToHost, s));
+        MOE_TRY(cudaStreamSynchronize(s));
+        *n_exact = n;
+    }
     return finish(cudaSuccess, ws, s);
 }
 

@@ -139,13 +139,9 @@ struct Work {
 // Work item w of the static schedule: expert-major, then N tile, then M tile.
 // ts is the table of TILE_ROWS-row tiles; this CTA's rows start `sub` rows into
 // the tile (a pair's rank-1 CTA: 128) and may be none (rows <= 0).
-#ifndef MOE_EXP_GEMM1_ORDER
-#define MOE_EXP_GEMM1_ORDER 0
-#endif
-template <int TILE_ROWS, int ORDER = 0>
+template <int TILE_ROWS>
 __device__ __forceinline__ Work decode_work(int w, int n_tiles, const int* ts, const int* offs, int G, int sub)
 {
-    if (ORDER == 1) w = ts[G] * n_tiles - 1 - w;
     int lo = 0, hi = G;   // ts[lo]*n <= w < ts[hi]*n
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -155,14 +151,8 @@ __device__ __forceinline__ Work decode_work(int w, int n_tiles, const int* ts, c
     r.g = lo;
     const int mt = ts[lo + 1] - ts[lo];
     const int wl = w - ts[lo] * n_tiles;
-    int ml;
-    if (ORDER == 2) {
-        ml = wl / n_tiles;
-        r.n_tile = wl - ml * n_tiles;
-    } else {
-        r.n_tile = wl / mt;
-        ml = wl - r.n_tile * mt;
-    }
+    r.n_tile = wl / mt;
+    const int ml = wl - r.n_tile * mt;
     r.row0 = offs[lo] + ml * TILE_ROWS + sub;
     r.rows = min(BM, offs[lo + 1] - r.row0);
     return r;
@@ -193,7 +183,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     constexpr bool COMBINE = (MODE == kGemm1Combine || MODE == kFusedCombine);
     constexpr bool CP_GATHER = (MODE == kGemm0CpGather);
     constexpr bool GATHER = (MODE == kGemm0Gather);
-    constexpr int G1_ORDER = (MODE == kGemm1Scatter || MODE == kGemm1Combine) ? MOE_EXP_GEMM1_ORDER : 0;
     static_assert(!PAIR || MODE == kGemm0Dense || MODE == kGemm1Scatter || MODE == kGemm1Combine,
                   "CTA pairs run the dense-A GEMM0 and the GEMM1 modes");
     static_assert(!PAIR || BK == 64, "CTA pairs use 128-byte rows of A");
@@ -322,8 +311,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const bool p1 = FUSED && w >= total0;
             const int n_tiles = p1 ? n_tiles1 : n_tiles0;
             const int k_blocks = p1 ? k_blocks1 : k_blocks0;
-            const Work wk = decode_work<C::TILE_ROWS, G1_ORDER>(p1 ? w - total0 : w, n_tiles, st->tile_start,
-                                                               st->offsets, G, sub);
+            const Work wk = decode_work<C::TILE_ROWS>(p1 ? w - total0 : w, n_tiles, st->tile_start, st->offsets,
+                                                     G, sub);
             if (p1) {
                 // the rows of h this tile reads: every GEMM0 tile of (expert, M tile)
                 // must have stored and published them
@@ -666,8 +655,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int w = unit; w < total; w += n_units) {
             const bool p1 = FUSED && w >= total0;
             const int n_tiles = p1 ? n_tiles1 : n_tiles0;
-            const Work wk = decode_work<C::TILE_ROWS, G1_ORDER>(p1 ? w - total0 : w, n_tiles, st->tile_start,
-                                                               st->offsets, G, sub);
+            const Work wk = decode_work<C::TILE_ROWS>(p1 ? w - total0 : w, n_tiles, st->tile_start, st->offsets,
+                                                     G, sub);
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&st->tfull[acc]), acc_phase, abort, args.err)))
                 break;
             tc_fence_after();

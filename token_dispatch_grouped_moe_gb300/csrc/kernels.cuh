@@ -42,6 +42,31 @@ cudaError_t launch_route(const RouteArgs& a, int num_sms, cudaStream_t s);
 // has_logits: a [T,E] logits scratch is passed (the layer call).
 int route_variant(int32_t H, int32_t E, bool has_logits);
 
+// The tensor-core router (route_tc.cu): the gate GEMM on tcgen05, each
+// token's selection proven equal to the canonical fp32 order's by an error
+// bound, or recomputed in that order. Scratch from the layer's workspace.
+constexpr int64_t kRouteTcMinTokens = 512;   // below: one tile per CTA is too few
+struct RouteTcArgs {
+    uint16_t* wgt;          // [NP, H] the gate transposed (NP = E rounded up to 16)
+    float* wpart;           // [H/64, NP] sums of squares of the gate's columns per 64 rows, rounded up
+    float* fast;            // [T, E] the tensor-core logits (bias added)
+    float* bound;           // [T] B_t: |fast - canonical| <= B_t for every expert of token t
+    int32_t* n_exact;       // tokens listed for the canonical recomputation (a count)
+    int32_t* flag_tok;      // [T] the listed tokens
+    uint64_t* flag_cand;    // [T] their run members (bit e)
+    int32_t* flag_sel;      // [T, 9] their top k+1 by fast logit
+    float* flag_selv;       // [T, 9] and those fast logits
+    float c_fast = 0.0f;    // bound constants (set by the launcher)
+    float c_tot = 0.0f;
+    float xx_infl = 1.0f;
+    int32_t force_exact = 0;     // recompute every token (test hook)
+    float* dbg_fast = nullptr;   // [T, E] the fast logits before the bias (test hook), or null
+    float* dbg_bound = nullptr;  // [T] c_fast ||x_t|| max_e ||w_e|| (test hook)
+};
+bool route_tc_supported(int64_t T, int32_t H, int32_t E);
+int route_tc_np(int32_t E);
+cudaError_t launch_route_tc(const RouteArgs& a, RouteTcArgs c, int num_sms, cudaStream_t s);
+
 // A TMA tensor map of a row-major bf16 matrix [outer, inner] with box
 // {box_inner, box_outer}, a 128- or 64-byte swizzle or none (swizzle_bytes
 // 128, 64 or 0); out-of-bounds elements

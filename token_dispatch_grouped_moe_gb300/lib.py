@@ -24,7 +24,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_set_option",
            "moe_get_option", "moe_permute_static", "moe_route_ex", "moe_layer_forward_ex",
-           "moe_layer_plan", "moe_selftest_wait_timeout", "moe_launch_count"]
+           "moe_layer_plan", "moe_selftest_wait_timeout", "moe_launch_count", "moe_selftest_route_tc"]
 
 OPT_GEMM0_A = 0
 GEMM0_A_PERMUTED = 0      # dispatch copies token rows to x_perm; GEMM0 loads dense tiles
@@ -46,6 +46,10 @@ OPT_X_PERM_COPY = 4
 X_PERM_COPY_AUTO = 0      # by the library's table
 X_PERM_COPY_INLINE = 1    # GEMM0's copy warps fill x_perm while the GEMM runs
 X_PERM_COPY_KERNEL = 2    # a copy kernel before GEMM0
+OPT_ROUTER = 5
+ROUTER_OPT_AUTO = 0       # by the library's table
+ROUTER_OPT_FMA = 1        # the FMA routers (the canonical order itself)
+ROUTER_OPT_TENSOR = 2     # the tensor-core router wherever it applies
 
 
 class MoeError(RuntimeError):
@@ -80,7 +84,7 @@ class Plan(ctypes.Structure):
                                               "cta_group_gemm1", "x_perm_copy")]
 
 
-ROUTER_STREAM, ROUTER_SLICED, ROUTER_CLUSTER, ROUTER_BLOCK = 0, 1, 2, 3
+ROUTER_STREAM, ROUTER_SLICED, ROUTER_CLUSTER, ROUTER_BLOCK, ROUTER_TENSOR = 0, 1, 2, 3, 4
 
 
 _lib = None
@@ -128,6 +132,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                          ctypes.POINTER(RoutingOut), P, sz, ctypes.POINTER(StageEvents), P]
     lib.moe_selftest_wait_timeout.restype = ctypes.c_int
     lib.moe_selftest_wait_timeout.argtypes = [i32, P]
+    lib.moe_selftest_route_tc.restype = ctypes.c_int
+    lib.moe_selftest_route_tc.argtypes = [D, P, P, P, i32, i32, P, P, P, P, ctypes.POINTER(ctypes.c_int64),
+                                          P, sz, P]
     lib.moe_layer_plan.restype = ctypes.c_int
     lib.moe_layer_plan.argtypes = [D, ctypes.POINTER(Plan)]
     lib.moe_layer_forward.restype = ctypes.c_int
@@ -194,6 +201,30 @@ def set_x_perm_copy(mode: int) -> None:
 
 def get_x_perm_copy() -> int:
     return int(load().moe_get_option(OPT_X_PERM_COPY))
+
+
+def set_router(mode: int) -> None:
+    """Which router the layer call runs (ROUTER_OPT_AUTO / _FMA / _TENSOR)."""
+    _ok(load().moe_set_option(OPT_ROUTER, int(mode)), "moe_set_option")
+
+
+def route_tc_selftest(dims: Dims, x, Wg, ws, bias=None, renormalize=True, force_exact=False,
+                      want_fast=False, stream=None):
+    """The tensor-core router alone (test hook moe_selftest_route_tc).
+    Returns (topk_idx, topk_w, fast_logits or None, fast_bound or None,
+    number of tokens recomputed in the canonical order)."""
+    T, k, E = dims.T, dims.k, dims.E
+    dev = x.device
+    idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    fast = torch.empty(T, E, dtype=torch.float32, device=dev) if want_fast else None
+    bound = torch.empty(T, dtype=torch.float32, device=dev) if want_fast else None
+    n = ctypes.c_int64(0)
+    _ok(load().moe_selftest_route_tc(ctypes.byref(dims), _p(x), _p(Wg), _p(bias), int(renormalize),
+                                     int(force_exact), _p(idx), _p(w), _p(fast), _p(bound),
+                                     ctypes.byref(n), _p(ws), ws.numel(), _stream(stream)),
+        "moe_selftest_route_tc")
+    return idx, w, fast, bound, int(n.value)
 
 
 def launch_count() -> int:
