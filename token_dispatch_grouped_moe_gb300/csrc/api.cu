@@ -16,7 +16,7 @@
 namespace moe {
 namespace {
 
-constexpr int kVersion = 200;   // 0.2.0
+constexpr int kVersion = 300;   // 0.3.0
 constexpr int kMaxDevices = 64;
 
 // ------------------------------------------------------------ device info --

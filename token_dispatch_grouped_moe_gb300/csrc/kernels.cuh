@@ -58,7 +58,6 @@ struct RouteTcArgs {
     float* flag_selv;       // [T, 9] and those fast logits
     float c_fast = 0.0f;    // bound constants (set by the launcher)
     float c_tot = 0.0f;
-    float xx_infl = 1.0f;
     int32_t force_exact = 0;     // recompute every token (test hook)
     float* dbg_fast = nullptr;   // [T, E] the fast logits before the bias (test hook), or null
     float* dbg_bound = nullptr;  // [T] c_fast ||x_t|| max_e ||w_e|| (test hook)

@@ -14,15 +14,14 @@
 //      per expert, zero rows up to NP = E rounded up to 16) and the sums of
 //      squares from which each column's 2-norm ||w_e|| follows, rounded up.
 //   2. route_tc_kernel: per 128-token tile, TMA streams x and WgT through an
-//      8-stage ring; one thread issues one tcgen05.mma per K = 16 step whose
-//      B operand is the x tile followed by the gate tile, so that a fresh
-//      TMEM partial over every 128 of H (two k-blocks, eight MMAs) holds both
-//      x x^T (128 columns) and the logits (NP columns). The epilogue warps
-//      (one thread per token) add the partials in fp32 in k order: the fast
-//      logit f_e, and from the diagonal of x x^T, ||x_t||^2.
+//      8-stage ring; one thread issues tcgen05.mma (K = 16) into a fresh TMEM
+//      partial [128 x NP] every 64 of H (one k-block, four MMAs). The
+//      epilogue warps (one thread per token) add the partials in fp32 in k
+//      order, the fast logit f_e, and read their token's row of each x tile
+//      from shared memory for ||x_t||^2 (fp32, every step rounded upward).
 //   3. The bound. With p_h = x_h w_he (exact in fp32) and S = sum_h p_h:
 //        canonical:  |l - S| <= gamma(H/32 + 5) sum|p|        (fp32 RN)
-//        fast:       |f - S| <= (8 u_mma + gamma(H/128)) sum|p|
+//        fast:       |f - S| <= (4 u_mma + gamma(H/64)) sum|p|
 //      where u_mma bounds one K = 16 tensor-core step relative to the
 //      magnitudes it adds (|C| + sum |a_i b_i|): products exact, then at most
 //      17 terms aligned and truncated to fp32, 2^-18 taken (twice the 17 *
@@ -62,23 +61,20 @@ constexpr int kTcBK = 64;         // k-block (one 128-byte swizzle row of bf16)
 constexpr int kTcStages = 8;
 constexpr int kTcThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTcABytes = kTcTile * kTcBK * 2;   // 16 KB
-constexpr int kTcXCols = 128;     // x x^T accumulator columns (one buffer)
-constexpr int kTcPartKB = 2;      // k-blocks per TMEM partial (8 MMAs of K = 16)
+constexpr int kTcPartKB = 1;      // k-blocks per TMEM partial (4 MMAs of K = 16)
 constexpr int kTcPrepRows = 64;   // gate rows per block of the prep kernel
 
-// One MMA per K = 16 step computes both products: B is the stage's x tile
-// (128 rows) followed by its gate tile (NP rows), one K-major 128-byte-swizzled
-// operand of N = 128 + NP rows, so D columns 0..127 hold x x^T and columns
-// 128.. the logits. A partial buffer is that many TMEM columns, rounded up to
-// a multiple of 32.
+// A stage holds the x tile (128 token rows x 64 of H) and the gate tile (NP
+// expert rows x 64 of H), both K-major in 128-byte-swizzled rows; one MMA per
+// K = 16 step multiplies them into a TMEM partial of NP columns. A partial
+// buffer is NP columns rounded up to a multiple of 32.
 template <int NP>
 struct TcCfg {
     static constexpr int B_BYTES = NP * kTcBK * 2;
     static constexpr int STAGE = kTcABytes + B_BYTES;   // a multiple of 1024
-    static constexpr int N = kTcXCols + NP;
-    static constexpr int PB_COLS = (N + 31) / 32 * 32;
-    static constexpr int NB = 512 / PB_COLS;
-    static constexpr uint32_t IDESC = idesc_bf16_f32(kTcTile, N, false, false);
+    static constexpr int PB_COLS = (NP + 31) / 32 * 32;
+    static constexpr int NB = 512 / PB_COLS > 8 ? 8 : 512 / PB_COLS;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(kTcTile, NP, false, false);
     static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
     static_assert(NB >= 2 && NB <= 8, "two to eight partial buffers");
 };
@@ -181,7 +177,9 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     if (threadIdx.x == 0) {
         for (int s = 0; s < kTcStages; ++s) {
             mbar_init(smem_u32(&st->full[s]), 1);
-            mbar_init(smem_u32(&st->empty[s]), 1);
+            // freed by the MMA's commit and by the four epilogue warps, which
+            // read their token rows of x from the stage (||x_t||^2)
+            mbar_init(smem_u32(&st->empty[s]), 5);
         }
         for (int b = 0; b < C::NB; ++b) {
             mbar_init(smem_u32(&st->pfull[b]), 1);
@@ -201,20 +199,6 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     }
     pdl_wait();
     pdl_launch_dependents();
-    if (warp == 2) {
-        // the largest column norm of the gate: the prep kernel's per-block sums
-        // of squares added in block order and the square root, all rounded
-        // upward (an upper bound)
-        const int nblk = a.H / kTcPrepRows;
-        float m = 0.0f;
-        for (int e = lane; e < E; e += 32) {
-            float ss = 0.0f;
-            for (int b = 0; b < nblk; ++b) ss = __fadd_ru(ss, c.wpart[(int64_t)b * NP + e]);
-            m = fmaxf(m, __fsqrt_ru(ss));
-        }
-        for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
-        if (lane == 0) st->wmax = m;
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -268,13 +252,14 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                     }
                     tc_fence_after();
                     const uint32_t a_base = tiles + stage * C::STAGE;
+                    const uint32_t b_base = a_base + kTcABytes;
                     const uint32_t d = tmem + pb * C::PB_COLS;
                     const bool part_end = in_part == kTcPartKB - 1 || kb == n_kb - 1;
 #pragma unroll
                     for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                        // A = the x tile; B = the x tile and the gate tile after it
                         const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
-                        tc_mma_f16<1>(d, ad, ad, C::IDESC, (in_part | kk) != 0 ? 1u : 0u);
+                        const uint64_t bd = smem_desc_sw128(b_base + kk * 32, 16, 1024);
+                        tc_mma_f16<1>(d, ad, bd, C::IDESC, (in_part | kk) != 0 ? 1u : 0u);
                     }
                     any = true;
                     tc_commit<1>(smem_u32(&st->empty[stage]));
@@ -294,10 +279,27 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         const int ew = warp & 3;   // TMEM lane quarter of this warp
         const int r = ew * 32 + lane;
         const uint32_t lane_off = (uint32_t)(ew * 32) << 16;
+        if (warp == 2) {
+            // the largest column norm of the gate: the prep kernel's per-block
+            // sums of squares added in block order and the square root, all
+            // rounded upward (an upper bound); computed while the first tile
+            // streams in, shared with the other epilogue warps by a named barrier
+            const int nblk = a.H / kTcPrepRows;
+            float m = 0.0f;
+            for (int e = lane; e < E; e += 32) {
+                float ss = 0.0f;
+                for (int b = 0; b < nblk; ++b) ss = __fadd_ru(ss, c.wpart[(int64_t)b * NP + e]);
+                m = fmaxf(m, __fsqrt_ru(ss));
+            }
+            for (int sh = 16; sh > 0; sh >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, sh));
+            if (lane == 0) st->wmax = m;
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
         const float wmax = st->wmax;
         const int n_part = (n_kb + kTcPartKB - 1) / kTcPartKB;
-        int pb = 0;
-        uint32_t pphase = 0;
+        int pb = 0, xstage = 0;
+        uint32_t pphase = 0, xphase = 0;
+        const unsigned char* tiles_ptr = smem_raw + (tiles - raw);
         for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
             float s[NP];
 #pragma unroll
@@ -305,18 +307,42 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
             float sumsq = 0.0f;
             bool ok = true;
             for (int q = 0; q < n_part; ++q) {
+                // this thread's token row of the stage's x tile: ||x_t||^2 in
+                // fp32 with every step rounded upward (never below the exact sum)
+                for (int u = 0; u < kTcPartKB; ++u) {
+                    if (q * kTcPartKB + u >= n_kb) break;
+                    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&st->full[xstage]), xphase, abort, a.err))) {
+                        ok = false;
+                        break;
+                    }
+                    const unsigned char* row = tiles_ptr + (size_t)xstage * C::STAGE + r * 128;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const float lo = __uint_as_float(w4[h] << 16), hi = __uint_as_float(w4[h] & 0xFFFF0000u);
+                            sumsq = __fmaf_ru(lo, lo, sumsq);
+                            sumsq = __fmaf_ru(hi, hi, sumsq);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&st->empty[xstage]));
+                    if (++xstage == kTcStages) { xstage = 0; xphase ^= 1u; }
+                }
+                if (!ok) break;
                 if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&st->pfull[pb]), pphase, abort, a.err))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t src = tmem + lane_off + pb * C::PB_COLS;
-                uint32_t dg[32], v[NP];
-                tmem_ld_32x32b_x32(src + ew * 32, dg);   // this warp's rows of x x^T: the diagonal
+                uint32_t v[NP];
 #pragma unroll
                 for (int u = 0; u + 32 <= NP; u += 32)
-                    tmem_ld_32x32b_x32(src + kTcXCols + u, *reinterpret_cast<uint32_t(*)[32]>(v + u));
-                if (NP % 32) tmem_ld_x16(src + kTcXCols + (NP / 32) * 32, v + (NP / 32) * 32);
+                    tmem_ld_32x32b_x32(src + u, *reinterpret_cast<uint32_t(*)[32]>(v + u));
+                if (NP % 32) tmem_ld_x16(src + (NP / 32) * 32, v + (NP / 32) * 32);
                 tc_wait_ld();
                 tc_fence_before();
                 __syncwarp();
@@ -324,28 +350,26 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
                 // the fp32 sums of the partials, in k order
 #pragma unroll
                 for (int e = 0; e < NP; ++e) s[e] = s[e] + __uint_as_float(v[e]);
-                float d = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (i == lane) d = __uint_as_float(dg[i]);
-                sumsq = sumsq + d;
                 if (++pb == C::NB) { pb = 0; pphase ^= 1u; }
             }
             if (!ok) break;
             const int64_t t = (int64_t)tile * kTcTile + r;
             if (t >= a.T) continue;
-            // ||x_t|| rounded up (sumsq adds positive terms: its relative
-            // error is below xx_infl - 1), then B_t
-            const float xnorm = sqrtf(fmaxf(sumsq, 0.0f) * c.xx_infl) * (1.0f + 0x1p-20f);
+            // ||x_t|| rounded up, then B_t
+            const float xnorm = __fsqrt_ru(sumsq);
             float fmax_abs = 0.0f;
-            float* dst = c.fast + t * E;
+            float4* dst = reinterpret_cast<float4*>(c.fast + t * E);   // E % 8 == 0: 32-byte aligned rows
 #pragma unroll
-            for (int e = 0; e < NP; ++e) {
+            for (int e = 0; e < NP; e += 4) {
                 if (e >= E) break;
-                float v = s[e];
-                if (a.bias) v = v + a.bias[e];
-                fmax_abs = fmaxf(fmax_abs, fabsf(v));
-                dst[e] = v;
+                float v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    v[u] = s[e + u];
+                    if (a.bias) v[u] = v[u] + a.bias[e + u];
+                    fmax_abs = fmaxf(fmax_abs, fabsf(v[u]));
+                }
+                dst[e / 4] = make_float4(v[0], v[1], v[2], v[3]);
             }
             float bnd = c.c_tot * xnorm * wmax * (1.0f + 0x1p-16f);
             // the bias add on either side rounds once more
@@ -659,8 +683,6 @@ void tc_constants(int32_t H, RouteTcArgs* c)
     const double cc = gamma(H / 32.0 + 5.0);
     c->c_fast = (float)(cf * (1.0 + 1e-6));
     c->c_tot = (float)((cf + cc) * (1.0 + 1e-6));
-    // x x^T: partials of positive terms (steps MMA steps each), added in fp32
-    c->xx_infl = (float)((1.0 + chain) * (1.0 + gamma(n_part)) * (1.0 + 1e-6));
 }
 
 template <int NP>
