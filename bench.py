@@ -44,7 +44,11 @@ METRIC = "MoE layer fwd bf16 TFLOP/s & tokens/s on 1 GB300; % of tensor peak / H
 # as it is now, keyed by (configuration, CTAs per MMA, who fills x_perm); kernels
 # without such a capture report null. (The captures of earlier forms of the kernel are
 # in the profile summaries.)
-GEMM0_TRAFFIC = {}
+GEMM0_TRAFFIC = {
+    # grouped_gemm_kernel<2, 1> (GEMM0 + SwiGLU, CTA pairs, dense x_perm tiles): 2911.1 MB read +
+    # 462.1 MB written, profiles/launches_mixtral_layer.md
+    ("mixtral", 2, "kernel"): 3_373_200_000,
+}
 L2_FLUSH_BYTES = 256 << 20
 
 
