@@ -14,7 +14,7 @@
 //      per expert, zero rows up to NP = E rounded up to 16) and the sums of
 //      squares from which each column's 2-norm ||w_e|| follows, rounded up.
 //   2. route_tc_kernel: per 128-token tile, TMA streams x and WgT through an
-//      8-stage ring; one thread issues tcgen05.mma (K = 16) into a fresh TMEM
+//      ring of 8 stages (4 when two CTAs share an SM); one thread issues tcgen05.mma (K = 16) into a fresh TMEM
 //      partial [128 x NP] every 64 of H (one k-block, four MMAs). The
 //      epilogue warps (one thread per token) add the partials in fp32 in k
 //      order, the fast logit f_e, and read their token's row of each x tile
@@ -58,7 +58,8 @@ namespace {
 
 constexpr int kTcTile = 128;      // tokens per tile (MMA M)
 constexpr int kTcBK = 64;         // k-block (one 128-byte swizzle row of bf16)
-constexpr int kTcStages = 8;
+constexpr int kTcStagesMax = 8;   // one CTA per SM: 8 stages; two CTAs per SM: 4 each
+constexpr int kTcTmemCols = 256;  // up to two CTAs per SM share the 512 TMEM columns
 constexpr int kTcThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTcABytes = kTcTile * kTcBK * 2;   // 16 KB
 constexpr int kTcPartKB = 1;      // k-blocks per TMEM partial (4 MMAs of K = 16)
@@ -73,15 +74,15 @@ struct TcCfg {
     static constexpr int B_BYTES = NP * kTcBK * 2;
     static constexpr int STAGE = kTcABytes + B_BYTES;   // a multiple of 1024
     static constexpr int PB_COLS = (NP + 31) / 32 * 32;
-    static constexpr int NB = 512 / PB_COLS > 8 ? 8 : 512 / PB_COLS;
+    static constexpr int NB = kTcTmemCols / PB_COLS > 8 ? 8 : kTcTmemCols / PB_COLS;
     static constexpr uint32_t IDESC = idesc_bf16_f32(kTcTile, NP, false, false);
     static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned");
     static_assert(NB >= 2 && NB <= 8, "two to eight partial buffers");
 };
 
 struct TcSmem {
-    uint64_t full[kTcStages];
-    uint64_t empty[kTcStages];
+    uint64_t full[kTcStagesMax];
+    uint64_t empty[kTcStagesMax];
     uint64_t pfull[8];
     uint64_t pempty[8];
     uint64_t drain;
@@ -90,10 +91,10 @@ struct TcSmem {
     float wmax;
 };
 
-template <int NP>
+template <int NP, int STAGES>
 constexpr size_t tc_smem_bytes()
 {
-    return 1024 + (size_t)kTcStages * TcCfg<NP>::STAGE + sizeof(TcSmem);
+    return 1024 + (size_t)STAGES * TcCfg<NP>::STAGE + sizeof(TcSmem);
 }
 
 // 32 lanes x 16 columns of 32-bit TMEM cells (thread i: lane base + i).
@@ -159,8 +160,8 @@ __global__ void __launch_bounds__(256) route_tc_prep_kernel(const uint16_t* __re
 
 // ------------------------------------------------------------------ main --
 
-template <int NP>
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int NP, int kTcStages>
+__global__ void __launch_bounds__(kTcThreads, 2)
 route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const RouteArgs a,
                 const RouteTcArgs c)
 {
@@ -194,7 +195,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         tma_prefetch_desc(&tmW);
     }
     if (warp == 1) {
-        tmem_alloc<1>(smem_u32(&st->tmem_base), 512);
+        tmem_alloc<1>(smem_u32(&st->tmem_base), kTcTmemCols);
         tmem_relinquish<1>();
     }
     pdl_wait();
@@ -388,7 +389,7 @@ route_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc<1>(tmem, 512);
+        tmem_dealloc<1>(tmem, kTcTmemCols);
     }
 }
 
@@ -594,6 +595,13 @@ __global__ void __launch_bounds__(256) route_tc_fix_kernel(const RouteArgs a, co
     for (int i = blockIdx.x * 8 + warp; i < n; i += gridDim.x * 8) {
         const int64_t t = c.flag_tok[i];
         const uint64_t cm = c.flag_cand[i];
+        // the token's top list, one entry per lane (gathered to lane 0 below)
+        int my_id = 0;
+        float my_v = 0.0f;
+        if (lane < kk1) {
+            my_id = c.flag_sel[(int64_t)i * 9 + lane];
+            my_v = c.flag_selv[(int64_t)i * 9 + lane];
+        }
         const uint16_t* xrow = a.x + t * a.H;
         uint64_t rest = cm;
         while (rest) {
@@ -612,13 +620,17 @@ __global__ void __launch_bounds__(256) route_tc_fix_kernel(const RouteArgs a, co
             }
         }
         __syncwarp();
+        float key[9];
+        int id[9];
+#pragma unroll
+        for (int j = 0; j < 9; ++j) {
+            id[j] = __shfl_sync(0xffffffffu, my_id, j);
+            key[j] = __shfl_sync(0xffffffffu, my_v, j);
+        }
         if (lane == 0) {
-            float key[9];
-            int id[9];
             uint64_t extra = cm;
             for (int j = 0; j < kk1; ++j) {
-                id[j] = c.flag_sel[(int64_t)i * 9 + j];
-                key[j] = ((cm >> id[j]) & 1ull) ? lg[id[j]] : c.flag_selv[(int64_t)i * 9 + j];
+                if ((cm >> id[j]) & 1ull) key[j] = lg[id[j]];
                 extra &= ~(1ull << id[j]);
             }
             int osel[8];
@@ -685,6 +697,21 @@ void tc_constants(int32_t H, RouteTcArgs* c)
     c->c_tot = (float)((cf + cc) * (1.0 + 1e-6));
 }
 
+template <int NP, int STAGES>
+cudaError_t launch_tc_s(const RouteArgs& a, const RouteTcArgs& c, const CUtensorMap& mx, const CUtensorMap& mw,
+                        int grid, cudaStream_t s)
+{
+    constexpr size_t smem = tc_smem_bytes<NP, STAGES>();
+    auto kern = route_tc_kernel<NP, STAGES>;
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(kern, dim3(grid), dim3(kTcThreads), smem, s, mx, mw, a, c);
+}
+
+// One CTA per 128-token tile: with at most one tile per SM, 8 stages in one
+// CTA; with more tiles, two CTAs of 4 stages share an SM, so that every tile
+// runs at once (measured: DeepSeek-shaped T = 32768, 256 tiles, main kernel
+// 34 -> 28 us; T = 16384, 128 tiles, 8 stages 4 us faster than 4).
 template <int NP>
 cudaError_t launch_tc(const RouteArgs& a, const RouteTcArgs& c, int num_sms, cudaStream_t s)
 {
@@ -692,13 +719,10 @@ cudaError_t launch_tc(const RouteArgs& a, const RouteTcArgs& c, int num_sms, cud
     if (!encode_map_2d(&mx, a.x, (uint64_t)a.H, (uint64_t)a.T, kTcBK, kTcTile, 128) ||
         !encode_map_2d(&mw, c.wgt, (uint64_t)a.H, (uint64_t)NP, kTcBK, NP, 128))
         return cudaErrorInvalidValue;
-    constexpr size_t smem = tc_smem_bytes<NP>();
-    auto kern = route_tc_kernel<NP>;
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (err != cudaSuccess) return err;
     const int64_t n_tiles = (a.T + kTcTile - 1) / kTcTile;
-    const int grid = (int)(n_tiles < num_sms ? n_tiles : num_sms);
-    return launch_pdl(kern, dim3(grid), dim3(kTcThreads), smem, s, mx, mw, a, c);
+    if (n_tiles <= num_sms) return launch_tc_s<NP, 8>(a, c, mx, mw, (int)n_tiles, s);
+    const int grid = (int)(n_tiles < 2 * num_sms ? n_tiles : 2 * num_sms);
+    return launch_tc_s<NP, 4>(a, c, mx, mw, grid, s);
 }
 
 }  // namespace
