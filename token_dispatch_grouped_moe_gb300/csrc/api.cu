@@ -9,6 +9,8 @@
 #include <cstring>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/moe.h"
 #include "kernels.cuh"
 #include "ptx.cuh"
@@ -18,6 +20,25 @@ namespace {
 
 constexpr int kVersion = 300;   // 0.3.0
 constexpr int kMaxDevices = 64;
+
+// ---------------------------------------------------------------- tracing --
+
+// An NVTX range over the host code that enqueues one stage: a profiler or
+// tracer that records NVTX (ncu --nvtx, Nsight Systems) attributes each
+// kernel to the stage that launched it ("moe/route", "moe/gemm0", ...). With
+// no tool attached, a push/pop pair is a couple of branches (NVTX v3 is
+// header-only and loads no library unless a tool asks for it).
+struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    void next(const char* name)   // close this range and open the next stage's
+    {
+        nvtxRangePop();
+        nvtxRangePushA(name);
+    }
+    Range(const Range&) = delete;
+    Range& operator=(const Range&) = delete;
+};
 
 // ------------------------------------------------------------ device info --
 
@@ -343,6 +364,7 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
         b.ready = ready;
         b.ready_target = 4 * ((F + 127) / 128);   // 4 epilogue warps x GEMM0 N tiles
         MOE_TRY(cudaMemsetAsync(ready, 0, (size_t)((M + kTileM - 1) / kTileM + G + 1) * 4, s));
+        Range r("moe/gemm0+gemm1");
         MOE_TRY(launch_grouped_gemm_fused(fc.on ? kFusedCombine : kFusedScatter, mx, m1, m3, mh, m2, a, b,
                                           sms, s));
         if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
@@ -355,8 +377,10 @@ moe_status run_expert_gemms(const moe_dims& d, int32_t M, int32_t F, int32_t G, 
         a.copy_ready = copy_ready;
         a.copy_dst = copy_dst;
     }
+    Range r("moe/gemm0");
     MOE_TRY(launch_grouped_gemm(dense ? kGemm0Dense : cp_gather ? kGemm0CpGather : kGemm0Gather, mx, m1,
                                 m3, a, sms, s, dense ? cta_group0 : 1));
+    r.next("moe/gemm1");
     a.copy_ready = nullptr;
     a.copy_dst = nullptr;
     if (ev_mid) MOE_TRY(cudaEventRecord((cudaEvent_t)ev_mid, s));
@@ -528,6 +552,7 @@ moe_status moe_route_ex(const moe_dims* dims, const moe_bf16* x, const moe_bf16*
     const int sms = num_sms_current();
     if (sms <= 0) return MOE_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
+    Range r("moe/route");
     RouteArgs a{x, Wg, bias, topk_idx, topk_w, dims->T, dims->H, dims->E, dims->k};
     a.renorm = gating ? (gating->renormalize != 0) : 1;
     return finish(launch_route(a, sms, s), nullptr, s);
@@ -551,6 +576,7 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* c
     PermuteArgs a{topk_idx, counts, offsets, src_row, inv_pos,
                   reinterpret_cast<int32_t*>(bytes(ws) + L.tile),
                   reinterpret_cast<int32_t*>(bytes(ws) + L.hist), err, R, dims->E};
+    Range r("moe/permute");
     MOE_TRY(launch_permute(a, s));
     if (x_perm)
         MOE_TRY(launch_gather_rows(x, src_row, offsets + dims->E, x_perm, R, dims->T, dims->H,
@@ -625,6 +651,7 @@ moe_status moe_combine(const moe_dims* dims, const float* slot, int32_t n_slots,
     const int sms = num_sms_current();
     if (sms <= 0) return MOE_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
+    Range r("moe/combine");
     return finish(launch_combine(slot, n_slots, out, dims->T, dims->H, sms, s), nullptr, s);
 }
 
@@ -684,6 +711,8 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     if (fused && d.F_shared == 0)
         MOE_TRY(cudaMemsetAsync(arrive, 0, (size_t)d.T * ((d.H + 255) / 256) * 4, s));
 
+    Range layer_range("moe/layer_forward");
+    Range stage("moe/route");
     record(events ? events->before_route : nullptr, s);
     RouteArgs ra{x, Wg, bias, idx, tw, d.T, d.H, d.E, d.k};
     ra.renorm = gating ? (gating->renormalize != 0) : 1;
@@ -694,6 +723,7 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     else
         MOE_TRY(launch_route(ra, sms, s));
 
+    stage.next("moe/permute");
     record(events ? events->before_permute : nullptr, s);
     PermuteArgs pa{idx, counts, offsets, src, inv, tile, reinterpret_cast<int32_t*>(w + L.hist), err,
                    R, d.E};
@@ -710,6 +740,7 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     // both routed GEMMs in one launch (dense A only)
     const bool fuse_gemms = plan.gemm_fusion == MOE_GEMM_FUSION_ON;
 
+    stage.next("moe/experts");
     record(events ? events->before_gemm0 : nullptr, s);
     MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)R, d.F, d.E, d.k, x, permuted ? xp : nullptr, src,
                                     tile, offsets, W1, W3, W2, tw, slot,
@@ -722,6 +753,7 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                                     copy_inline ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr,
                                     copy_inline ? xp : nullptr));
 
+    stage.next("moe/shared_expert");
     record(events ? events->before_shared : nullptr, s);
     if (d.F_shared > 0) {
         // the sigmoid gate, if any, is the shared expert's row weight in GEMM1
@@ -742,6 +774,7 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                                         cta_group_for(d.T, 1, true)));
     }
 
+    stage.next("moe/combine");
     record(events ? events->before_combine : nullptr, s);
     if (!fused)   // else GEMM1's epilogue finished it (the last contribution)
         MOE_TRY(launch_combine(slot, n_slots, out, d.T, d.H, sms, s));
