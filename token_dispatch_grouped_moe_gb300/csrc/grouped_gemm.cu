@@ -158,6 +158,71 @@ __device__ __forceinline__ Work decode_work(int w, int n_tiles, const int* ts, c
     return r;
 }
 
+// The fused combine of the rows whose (token, 256-column tile) this warp
+// finished (bit i of `todo`: lane i's row, token t on that lane): out[t, n0 +
+// 8l .. 8l+7] = bf16 of the left fold slot[0] + slot[1] + ... + slot[ns-1] in
+// fp32, lane l taking columns 8l .. 8l+7, for ns <= NS. Every slot load of a
+// batch of CB rows is issued before the first add, so a batch costs one
+// memory round trip (a fold that loads slot j only after adding slot j-1
+// costs ns of them).
+template <int NS, int CB>
+__device__ __forceinline__ void combine_rows(unsigned todo, int64_t t, const float* slot, uint16_t* out, int n0,
+                                             int N1, int64_t T, int ns)
+{
+    const int c = 8 * (threadIdx.x & 31);
+    const int64_t TN = T * (int64_t)N1;
+    const bool col_ok = n0 + c < N1;
+    while (todo) {
+        int64_t tt[CB];
+#pragma unroll
+        for (int u = 0; u < CB; ++u) {
+            tt[u] = -1;
+            if (todo) {   // warp-uniform: todo is a ballot
+                const int src_lane = __ffs(todo) - 1;
+                todo &= todo - 1;
+                tt[u] = __shfl_sync(0xffffffffu, t, src_lane);
+            }
+        }
+        if (!col_ok) continue;
+        float4 v[CB][NS][2];
+#pragma unroll
+        for (int u = 0; u < CB; ++u) {
+            if (tt[u] < 0) continue;
+            const float* src = slot + tt[u] * N1 + n0 + c;
+#pragma unroll
+            for (int j = 0; j < NS; ++j) {
+                if (j < ns) {
+                    v[u][j][0] = __ldcg(reinterpret_cast<const float4*>(src + j * TN));
+                    v[u][j][1] = __ldcg(reinterpret_cast<const float4*>(src + j * TN + 4));
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < CB; ++u) {
+            if (tt[u] < 0) continue;
+            float4 a0 = v[u][0][0], a1 = v[u][0][1];
+#pragma unroll
+            for (int j = 1; j < NS; ++j) {
+                if (j >= ns) break;
+                a0.x = a0.x + v[u][j][0].x; a0.y = a0.y + v[u][j][0].y;
+                a0.z = a0.z + v[u][j][0].z; a0.w = a0.w + v[u][j][0].w;
+                a1.x = a1.x + v[u][j][1].x; a1.y = a1.y + v[u][j][1].y;
+                a1.z = a1.z + v[u][j][1].z; a1.w = a1.w + v[u][j][1].w;
+            }
+            __nv_bfloat162 p0 = __floats2bfloat162_rn(a0.x, a0.y);
+            __nv_bfloat162 p1 = __floats2bfloat162_rn(a0.z, a0.w);
+            __nv_bfloat162 p2 = __floats2bfloat162_rn(a1.x, a1.y);
+            __nv_bfloat162 p3 = __floats2bfloat162_rn(a1.z, a1.w);
+            uint4 o;
+            o.x = *reinterpret_cast<uint32_t*>(&p0);
+            o.y = *reinterpret_cast<uint32_t*>(&p1);
+            o.z = *reinterpret_cast<uint32_t*>(&p2);
+            o.w = *reinterpret_cast<uint32_t*>(&p3);
+            *reinterpret_cast<uint4*>(out + tt[u] * N1 + n0 + c) = o;
+        }
+    }
+}
+
 template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
@@ -775,68 +840,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
                 // the warp sums its finished rows together: lane l takes columns
-                // 8l .. 8l+7, so each slot row is read as one coalesced 1 KB line;
-                // CB rows at a time, their loads issued together so that the
-                // L2 round trips of CB rows overlap
+                // 8l .. 8l+7, so each slot row is read as one coalesced 1 KB line
                 unsigned todo = __ballot_sync(0xffffffffu, last);
-                if (todo) __threadfence();
-                const int n0 = wk.n_tile * BN;
-                const int c = 8 * lane;
-                const int64_t TN = args.T * (int64_t)N1;
-                constexpr int CB = 4;
-                while (todo) {
-                    int64_t tt[CB];
-#pragma unroll
-                    for (int u = 0; u < CB; ++u) {
-                        tt[u] = -1;
-                        if (todo) {   // warp-uniform: todo is a ballot
-                            const int src_lane = __ffs(todo) - 1;
-                            todo &= todo - 1;
-                            tt[u] = __shfl_sync(0xffffffffu, t, src_lane);
-                        }
-                    }
-                    if (n0 + c < N1) {
-                        float4 a0[CB], a1[CB];
-#pragma unroll
-                        for (int u = 0; u < CB; ++u) {
-                            if (tt[u] < 0) continue;
-                            const float* src = slot + tt[u] * N1 + n0 + c;
-                            a0[u] = __ldcg(reinterpret_cast<const float4*>(src));
-                            a1[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
-                        }
-                        for (int jj = 1; jj < n_slots; ++jj) {
-                            float4 b0[CB], b1[CB];
-#pragma unroll
-                            for (int u = 0; u < CB; ++u) {
-                                if (tt[u] < 0) continue;
-                                const float* src = slot + tt[u] * N1 + n0 + c + jj * TN;
-                                b0[u] = __ldcg(reinterpret_cast<const float4*>(src));
-                                b1[u] = __ldcg(reinterpret_cast<const float4*>(src + 4));
-                            }
-#pragma unroll
-                            for (int u = 0; u < CB; ++u) {
-                                if (tt[u] < 0) continue;
-                                a0[u].x = a0[u].x + b0[u].x; a0[u].y = a0[u].y + b0[u].y;
-                                a0[u].z = a0[u].z + b0[u].z; a0[u].w = a0[u].w + b0[u].w;
-                                a1[u].x = a1[u].x + b1[u].x; a1[u].y = a1[u].y + b1[u].y;
-                                a1[u].z = a1[u].z + b1[u].z; a1[u].w = a1[u].w + b1[u].w;
-                            }
-                        }
-#pragma unroll
-                        for (int u = 0; u < CB; ++u) {
-                            if (tt[u] < 0) continue;
-                            __nv_bfloat162 p0 = __floats2bfloat162_rn(a0[u].x, a0[u].y);
-                            __nv_bfloat162 p1 = __floats2bfloat162_rn(a0[u].z, a0[u].w);
-                            __nv_bfloat162 p2 = __floats2bfloat162_rn(a1[u].x, a1[u].y);
-                            __nv_bfloat162 p3 = __floats2bfloat162_rn(a1[u].z, a1[u].w);
-                            uint4 o;
-                            o.x = *reinterpret_cast<uint32_t*>(&p0);
-                            o.y = *reinterpret_cast<uint32_t*>(&p1);
-                            o.z = *reinterpret_cast<uint32_t*>(&p2);
-                            o.w = *reinterpret_cast<uint32_t*>(&p3);
-                            *reinterpret_cast<uint4*>(out + tt[u] * N1 + n0 + c) = o;
-                        }
-                    }
+                if (todo) {
+                    __threadfence();
+                    const int n0 = wk.n_tile * BN;
+                    // batches: 4 rows of <= 2 slots, 2 rows of <= 6, else one row of <= 9
+                    if (n_slots <= 2) combine_rows<2, 4>(todo, t, slot, out, n0, N1, args.T, n_slots);
+                    else if (n_slots <= 6) combine_rows<6, 2>(todo, t, slot, out, n0, N1, args.T, n_slots);
+                    else combine_rows<9, 1>(todo, t, slot, out, n0, N1, args.T, n_slots);
                 }
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
