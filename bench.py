@@ -291,23 +291,27 @@ def bench_ours(args, cfg):
             stage_ms[n].append(t[j + 1] - t[j])
     stage_step_ms = float(np.mean([evs[0].elapsed_time(evs[-1]) for evs, _ in recs]))
 
-    # end to end through the C ABI with host buffers: x H2D, layer, out D2H
+    # end to end through the C ABI with host buffers (moe_layer_forward_host):
+    # x from pinned host memory, the layer, out back to pinned host memory,
+    # the token chunks' copies overlapping the kernels
     x_host = inp["x"].pin_memory()
     out_host = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
     x_dev = torch.empty_like(g["x"])
+    out_dev = torch.empty_like(g["x"])
+    host_chunks = args.host_chunks if args.host_chunks > 0 else lib.host_chunks(dims)
     e2e_ms = []
     for i in range(args.warmup + args.steps):
         flush.fill_(1)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        x_dev.copy_(x_host, non_blocking=True)
-        lib.layer_forward(dims, x_dev, g["Wg"], g["W1"], g["W3"], g["W2"], ws, W1s=g.get("W1s"),
-                          W3s=g.get("W3s"), W2s=g.get("W2s"), out=out)
-        out_host.copy_(out, non_blocking=True)
+        lib.layer_forward_host(dims, x_host, g["Wg"], g["W1"], g["W3"], g["W2"], ws, x_dev, out_dev, out_host,
+                               W1s=g.get("W1s"), W3s=g.get("W3s"), W2s=g.get("W2s"), n_chunks=host_chunks)
         e1.record(stream)
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_ms.append(e0.elapsed_time(e1))
+    if not torch.equal(out_dev, out):
+        raise RuntimeError("the host-buffer call's output differs from the device call's")
     e2e = max_over_ranks(float(np.mean(e2e_ms)), device)
 
     if rank != 0:
@@ -394,7 +398,8 @@ def bench_ours(args, cfg):
         "stage_roofline": stage_roofline,
         "e2e": {"value": round(world * flops / (e2e * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": cfg.T * cfg.H * 2,
-                "d2h_bytes_per_step": cfg.T * cfg.H * 2},
+                "d2h_bytes_per_step": cfg.T * cfg.H * 2, "call": "moe_layer_forward_host",
+                "chunks": host_chunks},
         "gpu_launches": launches,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 4),
@@ -538,6 +543,8 @@ def main():
                     help="x_perm filled inside GEMM0 while it runs, or by a kernel before it")
     ap.add_argument("--router", default="auto", choices=["auto", "fma", "tensor"],
                     help="the router kernels: the table's choice, the FMA routers, or the tensor-core router")
+    ap.add_argument("--host-chunks", type=int, default=0,
+                    help="token chunks of the end-to-end host-buffer call (0: the library's choice)")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work")
     ap.add_argument("--ref-tokens", type=int, default=64, help="oracle tokens per reference step")
     ap.add_argument("--stage", choices=["route", "permute"], default=None,

@@ -394,6 +394,41 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                                 const moe_routing_out* routing, void* ws, size_t ws_bytes,
                                 const moe_stage_events* events, moe_stream_t stream);
 
+/*
+ * The whole layer from and to host memory: x_host[T,H] in, out_host[T,H] out
+ * (bf16), every weight already on the device. The tokens are split into
+ * n_chunks consecutive chunks (0: the library's choice, else 1..64) and the
+ * chunks are pipelined: while the layer runs on chunk c (on `stream`), the
+ * host-to-device copy of chunk c+1 and the device-to-host copy of chunk c-1
+ * run on two copy streams the library keeps per device. Tokens are
+ * independent, so every output row is bit for bit the one
+ * moe_layer_forward gives for the whole batch (routing and the expert
+ * GEMMs of a row do not depend on the other rows in its chunk).
+ *
+ * x_host and out_host should be page-locked (cudaHostAlloc /
+ * cudaHostRegister); pageable memory works but its copies do not overlap.
+ * x_dev and out_dev are caller-owned device staging buffers of T*H bf16
+ * each, 16-byte aligned; on return x_dev holds x and out_dev the output.
+ * ws is moe_workspace_size(dims) bytes (the whole batch's), as for
+ * moe_layer_forward. The call is stream-ordered on `stream`: it starts after
+ * the work already queued there, and work queued there afterwards starts
+ * once out_host holds the result (synchronize the stream before reading it).
+ * Errors: the argument checks of moe_layer_forward (MOE_ERR_INVALID_ARG for
+ * a null or misaligned pointer or n_chunks outside 0..64); MOE_ERR_CUDA if a
+ * copy, an event or a launch fails, after which out_host is unspecified.
+ * Concurrent calls from several host threads on one device share the copy
+ * streams and are serialized by them (correct, not overlapped).
+ */
+moe_status moe_layer_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf16* Wg,
+                                  const float* bias, const moe_bf16* W1, const moe_bf16* W3,
+                                  const moe_bf16* W2, const moe_bf16* W1s, const moe_bf16* W3s,
+                                  const moe_bf16* W2s, moe_bf16* out_host, moe_bf16* x_dev,
+                                  moe_bf16* out_dev, int32_t n_chunks, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream);
+
+/* The chunk count moe_layer_forward_host uses for n_chunks = 0 (host only). */
+int32_t moe_host_chunks(const moe_dims* dims);
+
 #ifdef __cplusplus
 }
 #endif

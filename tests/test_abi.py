@@ -87,6 +87,40 @@ def test_host_validation_without_launch(L):
                                null) == 1
 
 
+def test_host_entry_validation_without_launch(L):
+    """moe_layer_forward_host rejects bad arguments before any copy or launch."""
+    from token_dispatch_grouped_moe_gb300 import lib
+    dummy = ctypes.c_void_p(256)
+    null = None
+    d = lib.make_dims(1000, 64, 64, 8, 2)
+    ws, need = ctypes.c_void_p(4096), lib.workspace_size(d)
+
+    def call(x_host=dummy, out_host=dummy, x_dev=dummy, out_dev=dummy, n_chunks=0, w=ws, nbytes=need):
+        return L.moe_layer_forward_host(ctypes.byref(d), x_host, dummy, null, dummy, dummy, dummy, null, null,
+                                        null, out_host, x_dev, out_dev, n_chunks, w, nbytes, null)
+
+    assert call(x_host=null) == 1
+    assert call(out_host=null) == 1
+    assert call(x_dev=null) == 1
+    assert call(out_dev=ctypes.c_void_p(264)) == 1   # staging buffers must be 16-byte aligned
+    assert call(n_chunks=-1) == 1
+    assert call(n_chunks=65) == 1
+    assert call(w=null) == 3
+    assert call(nbytes=need - 1) == 3
+    # no tokens: nothing to do, nothing touched
+    d0 = lib.make_dims(0, 64, 64, 8, 2)
+    assert L.moe_layer_forward_host(ctypes.byref(d0), null, null, null, null, null, null, null, null, null,
+                                    null, null, null, 0, ws, lib.workspace_size(d0), null) == 0
+
+
+def test_host_chunks_table(L):
+    """The library's chunk count: >= 8192 tokens a chunk, at most three."""
+    from token_dispatch_grouped_moe_gb300 import lib
+    for T, want in [(1, 1), (256, 1), (8191, 1), (8192, 1), (16383, 1), (16384, 2), (32768, 3), (65536, 3)]:
+        assert lib.host_chunks(lib.make_dims(T, 4096, 14336, 8, 2)) == want
+    assert L.moe_host_chunks(None) == 0
+
+
 def test_options(L):
     from token_dispatch_grouped_moe_gb300 import lib
     assert lib.get_gemm0_a() == lib.GEMM0_A_PERMUTED

@@ -8,6 +8,8 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
+#include <algorithm>
 
 #include <nvtx3/nvToolsExt.h>
 
@@ -417,6 +419,48 @@ bool debug_mode()
     return on;
 }
 
+// The two copy streams of moe_layer_forward_host (host-to-device and
+// device-to-host), created on first use for each device and kept until exit.
+struct CopyStreams {
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+};
+CopyStreams g_copy[kMaxDevices];
+std::mutex g_copy_mu;
+
+bool copy_streams(cudaStream_t* h2d, cudaStream_t* d2h)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lock(g_copy_mu);
+    CopyStreams& c = g_copy[dev];
+    if (!c.h2d && cudaStreamCreateWithFlags(&c.h2d, cudaStreamNonBlocking) != cudaSuccess) {
+        c.h2d = nullptr;
+        return false;
+    }
+    if (!c.d2h && cudaStreamCreateWithFlags(&c.d2h, cudaStreamNonBlocking) != cudaSuccess) {
+        c.d2h = nullptr;
+        return false;
+    }
+    *h2d = c.h2d;
+    *d2h = c.d2h;
+    return true;
+}
+
+// Chunks of moe_layer_forward_host when the caller leaves the choice to the
+// library: at least 8192 tokens each, at most three. A chunk pays the layer's
+// fixed costs again (launches, the GEMMs' last partial wave, another pass
+// over the expert weights), which a smaller chunk does not earn back through
+// the copies it hides. Measured on GB300 (ms per call, host link ~0.33 ms per
+// 64 MiB each way): Mixtral-shaped T = 8192: 1 chunk 3.97, 2 chunks 3.97,
+// 4 chunks 4.77 (the layer alone: 3.28 ms at T = 8192, 1.80 at T = 4096);
+// DeepSeek-shaped T = 32768: 1 chunk 3.99, 2: 3.47, 3: 3.42, 4: 3.50;
+// Qwen2-shaped T = 4096: 1 chunk 2.76, 2: 3.08.
+int32_t host_chunks_of(const moe_dims& d)
+{
+    const int64_t n = d.T / 8192;
+    return (int32_t)(n < 1 ? 1 : n > 3 ? 3 : n);
+}
+
 moe_status check_dims(const moe_dims* d)
 {
     if (!d) return MOE_ERR_INVALID_ARG;
@@ -779,6 +823,75 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     if (!fused)   // else GEMM1's epilogue finished it (the last contribution)
         MOE_TRY(launch_combine(slot, n_slots, out, d.T, d.H, sms, s));
     record(events ? events->after_combine : nullptr, s);
+    return finish(cudaSuccess, ws, s);
+}
+
+int32_t moe_host_chunks(const moe_dims* dims)
+{
+    if (check_dims(dims) != MOE_OK) return 0;
+    return host_chunks_of(*dims);
+}
+
+moe_status moe_layer_forward_host(const moe_dims* dims, const moe_bf16* x_host, const moe_bf16* Wg,
+                                  const float* bias, const moe_bf16* W1, const moe_bf16* W3,
+                                  const moe_bf16* W2, const moe_bf16* W1s, const moe_bf16* W3s,
+                                  const moe_bf16* W2s, moe_bf16* out_host, moe_bf16* x_dev,
+                                  moe_bf16* out_dev, int32_t n_chunks, void* ws, size_t ws_bytes,
+                                  moe_stream_t stream)
+{
+    MOE_TRY_STATUS(check_dims(dims));
+    MOE_TRY_STATUS(check_ws(*dims, ws, ws_bytes));
+    const moe_dims& d = *dims;
+    if (d.T == 0) return MOE_OK;
+    if (!x_host || !out_host || !x_dev || !out_dev) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_dev) || !aligned16(out_dev)) return MOE_ERR_INVALID_ARG;
+    if (n_chunks < 0 || n_chunks > 64) return MOE_ERR_INVALID_ARG;
+    Range range("moe/layer_forward_host");
+    const int32_t n = n_chunks == 0 ? host_chunks_of(d) : n_chunks;
+    // chunk c: tokens [c*base, min(T, (c+1)*base)), base a multiple of 128
+    int64_t base = (d.T + n - 1) / n;
+    base = (base + 127) / 128 * 128;
+    const int32_t n_used = (int32_t)((d.T + base - 1) / base);
+    cudaStream_t s = (cudaStream_t)stream, h2d = nullptr, d2h = nullptr;
+    if (!copy_streams(&h2d, &d2h)) return MOE_ERR_CUDA;
+    // events of this call (released by the runtime once they have completed)
+    std::vector<cudaEvent_t> ev(2 * (size_t)n_used + 2, nullptr);
+    struct Release {
+        std::vector<cudaEvent_t>& e;
+        ~Release()
+        {
+            for (cudaEvent_t x : e)
+                if (x) cudaEventDestroy(x);
+        }
+    } release{ev};
+    for (cudaEvent_t& e : ev) MOE_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
+    cudaEvent_t ev_start = ev[0], ev_done = ev[1];
+    // the copies start after the work already queued on the caller's stream
+    MOE_TRY(cudaEventRecord(ev_start, s));
+    MOE_TRY(cudaStreamWaitEvent(h2d, ev_start, 0));
+    MOE_TRY(cudaStreamWaitEvent(d2h, ev_start, 0));
+    const size_t row = (size_t)d.H * sizeof(moe_bf16);
+    for (int32_t c = 0; c < n_used; ++c) {
+        const int64_t t0 = c * base, tc = std::min<int64_t>(base, d.T - t0);
+        MOE_TRY(cudaMemcpyAsync(x_dev + t0 * d.H, x_host + t0 * d.H, (size_t)tc * row, cudaMemcpyHostToDevice,
+                                h2d));
+        MOE_TRY(cudaEventRecord(ev[2 + 2 * c], h2d));
+    }
+    for (int32_t c = 0; c < n_used; ++c) {
+        const int64_t t0 = c * base, tc = std::min<int64_t>(base, d.T - t0);
+        moe_dims dc = d;
+        dc.T = tc;
+        MOE_TRY(cudaStreamWaitEvent(s, ev[2 + 2 * c], 0));
+        MOE_TRY_STATUS(moe_layer_forward_ex(&dc, x_dev + t0 * d.H, Wg, bias, nullptr, W1, W3, W2, W1s, W3s, W2s,
+                                            out_dev + t0 * d.H, nullptr, ws, ws_bytes, nullptr, stream));
+        MOE_TRY(cudaEventRecord(ev[3 + 2 * c], s));
+        MOE_TRY(cudaStreamWaitEvent(d2h, ev[3 + 2 * c], 0));
+        MOE_TRY(cudaMemcpyAsync(out_host + t0 * d.H, out_dev + t0 * d.H, (size_t)tc * row, cudaMemcpyDeviceToHost,
+                                d2h));
+    }
+    // later work on the caller's stream waits for the last copy to the host
+    MOE_TRY(cudaEventRecord(ev_done, d2h));
+    MOE_TRY(cudaStreamWaitEvent(s, ev_done, 0));
     return finish(cudaSuccess, ws, s);
 }
 

@@ -24,7 +24,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_version", "moe_status_string", "moe_workspace_size", "moe_check", "moe_route",
            "moe_permute", "moe_expert_ffn", "moe_combine", "moe_layer_forward", "moe_set_option",
            "moe_get_option", "moe_permute_static", "moe_route_ex", "moe_layer_forward_ex",
-           "moe_layer_plan", "moe_selftest_wait_timeout", "moe_launch_count", "moe_selftest_route_tc"]
+           "moe_layer_plan", "moe_selftest_wait_timeout", "moe_launch_count", "moe_selftest_route_tc",
+           "moe_layer_forward_host", "moe_host_chunks"]
 
 OPT_GEMM0_A = 0
 GEMM0_A_PERMUTED = 0      # dispatch copies token rows to x_perm; GEMM0 loads dense tiles
@@ -140,6 +141,10 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.moe_layer_forward.restype = ctypes.c_int
     lib.moe_layer_forward.argtypes = [D, P, P, P, P, P, P, P, P, P, P, ctypes.POINTER(RoutingOut), P,
                                       sz, ctypes.POINTER(StageEvents), P]
+    lib.moe_layer_forward_host.restype = ctypes.c_int
+    lib.moe_layer_forward_host.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, P, i32, P, sz, P]
+    lib.moe_host_chunks.restype = i32
+    lib.moe_host_chunks.argtypes = [D]
     _lib = lib
     return lib
 
@@ -373,6 +378,25 @@ def layer_forward(dims: Dims, x, Wg, W1, W3, W2, ws, bias=None, W1s=None, W3s=No
                                         ctypes.byref(events) if events is not None else None,
                                         _stream(stream)), "moe_layer_forward_ex")
     return out
+
+
+def layer_forward_host(dims: Dims, x_host, Wg, W1, W3, W2, ws, x_dev, out_dev, out_host=None, bias=None,
+                       W1s=None, W3s=None, W2s=None, n_chunks=0, stream=None):
+    """moe_layer_forward_host: x_host and out_host in (pinned) host memory,
+    x_dev/out_dev device staging buffers of [T, H] bf16; the chunks' copies
+    overlap the layer's kernels. Returns out_host (valid once the stream has
+    been synchronized)."""
+    if out_host is None:
+        out_host = torch.empty(dims.T, dims.H, dtype=torch.bfloat16).pin_memory()
+    _ok(load().moe_layer_forward_host(ctypes.byref(dims), _p(x_host), _p(Wg), _p(bias), _p(W1), _p(W3), _p(W2),
+                                      _p(W1s), _p(W3s), _p(W2s), _p(out_host), _p(x_dev), _p(out_dev),
+                                      int(n_chunks), _p(ws), ws.numel(), _stream(stream)),
+        "moe_layer_forward_host")
+    return out_host
+
+
+def host_chunks(dims: Dims) -> int:
+    return int(load().moe_host_chunks(ctypes.byref(dims)))
 
 
 class MoELayer:
