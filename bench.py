@@ -155,8 +155,9 @@ def roofline_stage_bytes(cfg):
         "route": T * H * 2 + H * E * 2 + T * k * 8,
         "combine": n_slots * T * H * 4 + T * H * 2,
         "permute_index": R * 4 * 4 + E * 8,
-        # the dispatch with x_perm materialised: the routed rows read and written
-        "permute": 2 * R * H * 2,
+        # the dispatch with x_perm materialised: each token's row of x read once,
+        # each routed row of x_perm written once, and the index arrays
+        "permute": T * H * 2 + R * H * 2 + R * 4 * 4,
     }
 
 
@@ -467,7 +468,8 @@ def bench_reference(args, cfg):
 def bench_stage(args):
     """One stage through the C ABI at any shape (--T --H --E --k), outside the
     layer call: `route` (moe_route; T*H*2 + H*E*2 + T*k*8 bytes) or `permute`
-    (moe_permute with x_perm; 2*T*k*H*2 bytes). Before every timed call L2 is
+    (moe_permute with x_perm; T*H*2 + T*k*H*2 + T*k*16 bytes: x read once, x_perm
+    written, the index arrays). Before every timed call L2 is
     emptied of the inputs by writing and then reading a 256 MiB buffer (the
     read leaves L2 holding clean lines, so the timed call pays no write-back
     of the flush); each call is timed with CUDA events on the current stream.
@@ -515,7 +517,8 @@ def bench_stage(args):
     if ws is not None and lib.check(ws) != lib.MOE_OK:
         raise RuntimeError("device error in the stage calls")
     t = float(np.median(times))
-    work = T * H * 2 + H * E * 2 + T * k * 8 if args.stage == "route" else 2 * T * k * H * 2
+    work = (T * H * 2 + H * E * 2 + T * k * 8 if args.stage == "route"
+            else T * H * 2 + T * k * H * 2 + T * k * 4 * 4)
     peaks = measured_peaks()
     gbs = work / t / 1e9
     return {"stage": args.stage, "config": {"T": T, "H": H, "E": E, "k": k},

@@ -623,8 +623,8 @@ moe_status moe_permute(const moe_dims* dims, const int32_t* topk_idx, int32_t* c
     Range r("moe/permute");
     MOE_TRY(launch_permute(a, s));
     if (x_perm)
-        MOE_TRY(launch_gather_rows(x, src_row, offsets + dims->E, x_perm, R, dims->T, dims->H,
-                                   dims->k, err, sms, s));
+        MOE_TRY(launch_scatter_rows(x, topk_idx, inv_pos, offsets + dims->E, x_perm, dims->T, dims->H, dims->k,
+                                    dims->E, err, sms, s));
     return finish(cudaSuccess, ws, s);
 }
 
@@ -779,7 +779,7 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
     // x_perm: copied by GEMM0's copy warps while it runs, or by a kernel first
     const bool copy_inline = permuted && plan.x_perm_copy == MOE_X_PERM_COPY_INLINE;
     if (permuted && !copy_inline)
-        MOE_TRY(launch_gather_rows(x, src, offsets + d.E, xp, R, d.T, d.H, d.k, err, sms, s));
+        MOE_TRY(launch_scatter_rows(x, idx, inv, offsets + d.E, xp, d.T, d.H, d.k, d.E, err, sms, s));
 
     // both routed GEMMs in one launch (dense A only)
     const bool fuse_gemms = plan.gemm_fusion == MOE_GEMM_FUSION_ON;

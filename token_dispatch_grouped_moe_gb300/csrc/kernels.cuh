@@ -97,6 +97,11 @@ cudaError_t launch_permute(const PermuteArgs& a, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* src_row, const int32_t* r_valid,
                                uint16_t* x_perm, int64_t R, int64_t T, int32_t H, int32_t k,
                                uint32_t* err, int num_sms, cudaStream_t s);
+// The same x_perm from the token side: x[t] to x_perm[inv_pos[t*k + j]] for
+// every j whose id topk_idx[t*k + j] is in [0, E); x read once per token.
+cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* topk_idx, const int32_t* inv_pos,
+                                const int32_t* r_valid, uint16_t* x_perm, int64_t T, int32_t H, int32_t k,
+                                int32_t E, uint32_t* err, int num_sms, cudaStream_t s);
 
 cudaError_t launch_tile_table(const int32_t* offsets, int32_t G, int32_t* tile_start,
                               cudaStream_t s);

@@ -230,6 +230,56 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t
     }
 }
 
+// x_perm by token: a warp per token reads its row of x once and writes it to
+// the token's k dispatch positions (inv_pos[t*k + j], for the valid ids), 4 KB
+// of the row at a time in registers. Every x_perm row p < *r_valid is the
+// position of exactly one valid assignment, so each is written once, with the
+// same bytes as the gather by src_row; x is read once instead of k times.
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const uint16_t* __restrict__ x,
+                                                           const int32_t* __restrict__ topk_idx,
+                                                           const int32_t* __restrict__ inv_pos,
+                                                           const int32_t* __restrict__ r_valid,
+                                                           uint16_t* __restrict__ x_perm, int64_t T, int32_t H,
+                                                           int32_t k, int32_t E, uint32_t* err)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    constexpr int U = 8;   // 16-byte words a lane holds: 4 KB of the row per pass
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int vec_per_row = H / 8;
+    const int64_t n_valid = *r_valid;
+    for (int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += warps) {
+        // lane j < k: the position of assignment j of this token, or -1
+        int p = -1;
+        if (lane < k) {
+            const int id = topk_idx[t * k + lane];
+            if (id >= 0 && id < E) {
+                p = inv_pos[t * k + lane];
+                if (p < 0 || p >= n_valid) {
+                    report_error(err, MOE_DEV_ERR_BOUNDS);
+                    p = -1;
+                }
+            }
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+        for (int v0 = 0; v0 < vec_per_row; v0 += 32 * U) {
+            uint4 r[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (v0 + 32 * u + lane < vec_per_row) r[u] = __ldg(src + v0 + 32 * u + lane);
+            for (int j = 0; j < k; ++j) {
+                const int pj = __shfl_sync(0xffffffffu, p, j);
+                if (pj < 0) continue;
+                uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)pj * H);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (v0 + 32 * u + lane < vec_per_row) dst[v0 + 32 * u + lane] = r[u];
+            }
+        }
+    }
+}
+
 __global__ void tile_table_kernel(const int32_t* __restrict__ offsets, int32_t G,
                                   int32_t* __restrict__ tile_start)
 {
@@ -284,6 +334,17 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* src_row, const 
     const int grid = (int)(blocks_needed < (int64_t)num_sms * 8 ? blocks_needed : (int64_t)num_sms * 8);
     return launch_pdl(gather_rows_kernel, dim3(grid), dim3(256), 0, s, x, src_row, r_valid, x_perm, R, T, H, k,
                       err);
+}
+
+cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* topk_idx, const int32_t* inv_pos,
+                                const int32_t* r_valid, uint16_t* x_perm, int64_t T, int32_t H, int32_t k,
+                                int32_t E, uint32_t* err, int num_sms, cudaStream_t s)
+{
+    if (T == 0) return cudaSuccess;
+    const int64_t blocks_needed = (T + 7) / 8;
+    const int grid = (int)(blocks_needed < (int64_t)num_sms * 8 ? blocks_needed : (int64_t)num_sms * 8);
+    return launch_pdl(scatter_rows_kernel, dim3(grid), dim3(256), 0, s, x, topk_idx, inv_pos, r_valid, x_perm, T,
+                      H, k, E, err);
 }
 
 cudaError_t launch_tile_table(const int32_t* offsets, int32_t G, int32_t* tile_start, cudaStream_t s)
