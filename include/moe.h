@@ -401,9 +401,14 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
  * chunks are pipelined: while the layer runs on chunk c (on `stream`), the
  * host-to-device copy of chunk c+1 and the device-to-host copy of chunk c-1
  * run on two copy streams the library keeps per device. Tokens are
- * independent, so every output row is bit for bit the one
- * moe_layer_forward gives for the whole batch (routing and the expert
- * GEMMs of a row do not depend on the other rows in its chunk).
+ * independent (routing and the expert GEMMs of a row do not depend on the
+ * other rows in its chunk) and every chunk runs the router family the whole
+ * batch would, so every output row is bit for bit the one moe_layer_forward
+ * gives for the whole batch. One exception: when the whole batch takes the
+ * tensor-core router and a caller-chosen n_chunks leaves a chunk below the
+ * 512 tokens that router needs, that chunk takes the FMA routers: the same
+ * ids and dispatch, gate weights within fp32 rounding (the library's own
+ * chunk choice never does this).
  *
  * x_host and out_host should be page-locked (cudaHostAlloc /
  * cudaHostRegister); pageable memory works but its copies do not overlap.

@@ -44,6 +44,23 @@ CASES = [(1000, 256, 192, 8, 2, 0), (700, 256, 128, 16, 4, 256), (300, 128, 128,
          (8192, 512, 512, 8, 2, 0)]
 
 
+@pytest.mark.parametrize("n_chunks", [0, 2, 3])
+def test_host_call_keeps_the_batch_router(lib, n_chunks):
+    """A batch that takes the tensor-core router (E >= 16 from 8192 tokens)
+    in chunks of fewer tokens: each chunk still takes it, so the gate weights
+    and the output are the whole batch's bit for bit."""
+    T, H, F, E, k = 9000, 256, 128, 16, 2
+    dims = lib.make_dims(T, H, F, E, k)
+    assert lib.layer_plan(dims).router == lib.ROUTER_TENSOR
+    inp = make_inputs(T, H, F, E, seed=9)
+    g = {n: v.cuda() for n, v in inp.items()}
+    ws = lib.workspace(dims)
+    ref = lib.layer_forward(dims, g["x"], g["Wg"], g["W1"], g["W3"], g["W2"], ws)
+    torch.cuda.synchronize()
+    out = _host_call(lib, dims, inp, g, ws, n_chunks)
+    assert torch.equal(out.view(torch.int16), ref.cpu().view(torch.int16))
+
+
 @pytest.mark.parametrize("shape", CASES)
 @pytest.mark.parametrize("n_chunks", [0, 1, 2, 3, 8])
 def test_host_call_matches_layer(lib, shape, n_chunks):

@@ -477,6 +477,134 @@ moe_status check_dims(const moe_dims* d)
 
 }  // namespace moe
 
+namespace moe {
+
+// The layer call with an optional router override (router_force >= 0): the
+// host-buffer call runs every chunk with the router kernel family the whole
+// batch would take, so that a chunk's gate weights are the whole batch's
+// (the FMA routers share their bits; the tensor-core router's proven tokens
+// take weights from its own logits).
+moe_status layer_forward_impl(const moe_dims* dims, const moe_bf16* x, const moe_bf16* Wg, const float* bias,
+                              const moe_gating* gating, const moe_bf16* W1, const moe_bf16* W3,
+                              const moe_bf16* W2, const moe_bf16* W1s, const moe_bf16* W3s, const moe_bf16* W2s,
+                              moe_bf16* out, const moe_routing_out* routing, void* ws, size_t ws_bytes,
+                              const moe_stage_events* events, moe_stream_t stream, int router_force)
+{
+    MOE_TRY_STATUS(check_dims(dims));
+    MOE_TRY_STATUS(check_ws(*dims, ws, ws_bytes));
+    const moe_dims& d = *dims;
+    if (d.T == 0) return MOE_OK;
+    if (!x || !Wg || !W1 || !W3 || !W2 || !out) return MOE_ERR_INVALID_ARG;
+    if (d.F_shared > 0 && (!W1s || !W3s || !W2s)) return MOE_ERR_INVALID_ARG;
+    const void* ptrs[] = {x, Wg, W1, W3, W2, out};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (d.F_shared > 0 && (!aligned16(W1s) || !aligned16(W3s) || !aligned16(W2s)))
+        return MOE_ERR_INVALID_ARG;
+    const moe_bf16* shared_gate = gating ? gating->shared_gate : nullptr;
+    if (shared_gate && (d.F_shared == 0 || !aligned16(shared_gate))) return MOE_ERR_INVALID_ARG;
+    const int sms = num_sms_current();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    cudaStream_t s = (cudaStream_t)stream;
+    const Layout L = layout_of(d);
+    unsigned char* w = bytes(ws);
+    uint32_t* err = reinterpret_cast<uint32_t*>(w + L.err);
+    auto pick_i = [&](int32_t* user, size_t off) { return user ? user : reinterpret_cast<int32_t*>(w + off); };
+    int32_t* idx = pick_i(routing ? routing->topk_idx : nullptr, L.idx);
+    float* tw = (routing && routing->topk_w) ? routing->topk_w : reinterpret_cast<float*>(w + L.w);
+    int32_t* counts = pick_i(routing ? routing->counts : nullptr, L.counts);
+    int32_t* offsets = pick_i(routing ? routing->offsets : nullptr, L.offsets);
+    int32_t* src = pick_i(routing ? routing->src_row : nullptr, L.src);
+    int32_t* inv = pick_i(routing ? routing->inv_pos : nullptr, L.inv);
+    int32_t* tile = reinterpret_cast<int32_t*>(w + L.tile);
+    float* slot = reinterpret_cast<float*>(w + L.slot);
+    const int64_t R = d.T * d.k;
+    const int32_t n_slots = d.k + (d.F_shared > 0 ? 1 : 0);
+    int32_t* arrive = reinterpret_cast<int32_t*>(w + L.arrive);
+    moe_plan plan = plan_of(d);
+    if (router_force == MOE_ROUTER_TENSOR && route_tc_supported(d.T, d.H, d.E))
+        plan.router = MOE_ROUTER_TENSOR;
+    else if (router_force >= 0 && router_force != MOE_ROUTER_TENSOR)
+        plan.router = route_variant(d.H, d.E, /*has_logits=*/true);
+    const bool fused = plan.combine == MOE_COMBINE_FUSED;
+    // GEMM1 counts contributions per (token, 256-column tile); with a shared
+    // expert its GEMM1 runs last and is the only arrival (no counting)
+    if (fused && d.F_shared == 0)
+        MOE_TRY(cudaMemsetAsync(arrive, 0, (size_t)d.T * ((d.H + 255) / 256) * 4, s));
+
+    Range layer_range("moe/layer_forward");
+    Range stage("moe/route");
+    record(events ? events->before_route : nullptr, s);
+    RouteArgs ra{x, Wg, bias, idx, tw, d.T, d.H, d.E, d.k};
+    ra.renorm = gating ? (gating->renormalize != 0) : 1;
+    ra.err = err;
+    ra.logits = reinterpret_cast<float*>(w + L.logits);
+    if (plan.router == MOE_ROUTER_TENSOR)
+        MOE_TRY(launch_route_tc(ra, tc_args_of(L, w), sms, s));
+    else
+        MOE_TRY(launch_route(ra, sms, s));
+
+    stage.next("moe/permute");
+    record(events ? events->before_permute : nullptr, s);
+    PermuteArgs pa{idx, counts, offsets, src, inv, tile, reinterpret_cast<int32_t*>(w + L.hist), err,
+                   R, d.E};
+    MOE_TRY(launch_permute(pa, s));
+
+    const bool permuted = (plan.gemm0_a == MOE_GEMM0_A_PERMUTED);
+    const bool cp_gather = (plan.gemm0_a == MOE_GEMM0_A_CP_GATHER);
+    uint16_t* xp = reinterpret_cast<uint16_t*>(w + L.xp);
+    // x_perm: copied by GEMM0's copy warps while it runs, or by a kernel first
+    const bool copy_inline = permuted && plan.x_perm_copy == MOE_X_PERM_COPY_INLINE;
+    if (permuted && !copy_inline)
+        MOE_TRY(launch_scatter_rows(x, idx, inv, offsets + d.E, xp, d.T, d.H, d.k, d.E, err, sms, s));
+
+    // both routed GEMMs in one launch (dense A only)
+    const bool fuse_gemms = plan.gemm_fusion == MOE_GEMM_FUSION_ON;
+
+    stage.next("moe/experts");
+    record(events ? events->before_gemm0 : nullptr, s);
+    MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)R, d.F, d.E, d.k, x, permuted ? xp : nullptr, src,
+                                    tile, offsets, W1, W3, W2, tw, slot,
+                                    reinterpret_cast<uint16_t*>(w + L.h), err, sms, s,
+                                    events ? events->before_gemm1 : nullptr,
+                                    // with a shared expert, only its GEMM1 (the last) combines
+                                    FusedCombine{fused && d.F_shared == 0, 0, n_slots, arrive, out}, cp_gather,
+                                    fuse_gemms ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr,
+                                    plan.cta_group, plan.cta_group_gemm1,
+                                    copy_inline ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr,
+                                    copy_inline ? xp : nullptr));
+
+    stage.next("moe/shared_expert");
+    record(events ? events->before_shared : nullptr, s);
+    if (d.F_shared > 0) {
+        // the sigmoid gate, if any, is the shared expert's row weight in GEMM1
+        float* sgate = nullptr;
+        if (shared_gate) {
+            sgate = reinterpret_cast<float*>(w + L.sgate);
+            MOE_TRY(launch_shared_gate(x, shared_gate, sgate, d.T, d.H, sms, s));
+        }
+        // identity dispatch: every token, in token order, weight 1
+        MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)d.T, d.F_shared, 1, 1, x,
+                                        (permuted || cp_gather) ? x : nullptr,
+                                        nullptr, nullptr, nullptr, W1s, W3s, W2s, sgate,
+                                        fused ? slot : slot + (size_t)d.k * d.T * d.H,
+                                        reinterpret_cast<uint16_t*>(w + L.hs), err, sms, s, nullptr,
+                                        // every routed slot is written: one arrival each
+                                        FusedCombine{fused, d.k, n_slots, arrive, out, 1}, false, nullptr,
+                                        (permuted || cp_gather) ? cta_group_for(d.T, 1, false) : 1,
+                                        cta_group_for(d.T, 1, true)));
+    }
+
+    stage.next("moe/combine");
+    record(events ? events->before_combine : nullptr, s);
+    if (!fused)   // else GEMM1's epilogue finished it (the last contribution)
+        MOE_TRY(launch_combine(slot, n_slots, out, d.T, d.H, sms, s));
+    record(events ? events->after_combine : nullptr, s);
+    return finish(cudaSuccess, ws, s);
+}
+
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
@@ -717,113 +845,8 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
                                 const moe_routing_out* routing, void* ws, size_t ws_bytes,
                                 const moe_stage_events* events, moe_stream_t stream)
 {
-    MOE_TRY_STATUS(check_dims(dims));
-    MOE_TRY_STATUS(check_ws(*dims, ws, ws_bytes));
-    const moe_dims& d = *dims;
-    if (d.T == 0) return MOE_OK;
-    if (!x || !Wg || !W1 || !W3 || !W2 || !out) return MOE_ERR_INVALID_ARG;
-    if (d.F_shared > 0 && (!W1s || !W3s || !W2s)) return MOE_ERR_INVALID_ARG;
-    const void* ptrs[] = {x, Wg, W1, W3, W2, out};
-    for (const void* p : ptrs)
-        if (!aligned16(p)) return MOE_ERR_INVALID_ARG;
-    if (d.F_shared > 0 && (!aligned16(W1s) || !aligned16(W3s) || !aligned16(W2s)))
-        return MOE_ERR_INVALID_ARG;
-    const moe_bf16* shared_gate = gating ? gating->shared_gate : nullptr;
-    if (shared_gate && (d.F_shared == 0 || !aligned16(shared_gate))) return MOE_ERR_INVALID_ARG;
-    const int sms = num_sms_current();
-    if (sms <= 0) return MOE_ERR_CUDA;
-    cudaStream_t s = (cudaStream_t)stream;
-    const Layout L = layout_of(d);
-    unsigned char* w = bytes(ws);
-    uint32_t* err = reinterpret_cast<uint32_t*>(w + L.err);
-    auto pick_i = [&](int32_t* user, size_t off) { return user ? user : reinterpret_cast<int32_t*>(w + off); };
-    int32_t* idx = pick_i(routing ? routing->topk_idx : nullptr, L.idx);
-    float* tw = (routing && routing->topk_w) ? routing->topk_w : reinterpret_cast<float*>(w + L.w);
-    int32_t* counts = pick_i(routing ? routing->counts : nullptr, L.counts);
-    int32_t* offsets = pick_i(routing ? routing->offsets : nullptr, L.offsets);
-    int32_t* src = pick_i(routing ? routing->src_row : nullptr, L.src);
-    int32_t* inv = pick_i(routing ? routing->inv_pos : nullptr, L.inv);
-    int32_t* tile = reinterpret_cast<int32_t*>(w + L.tile);
-    float* slot = reinterpret_cast<float*>(w + L.slot);
-    const int64_t R = d.T * d.k;
-    const int32_t n_slots = d.k + (d.F_shared > 0 ? 1 : 0);
-    int32_t* arrive = reinterpret_cast<int32_t*>(w + L.arrive);
-    const moe_plan plan = plan_of(d);
-    const bool fused = plan.combine == MOE_COMBINE_FUSED;
-    // GEMM1 counts contributions per (token, 256-column tile); with a shared
-    // expert its GEMM1 runs last and is the only arrival (no counting)
-    if (fused && d.F_shared == 0)
-        MOE_TRY(cudaMemsetAsync(arrive, 0, (size_t)d.T * ((d.H + 255) / 256) * 4, s));
-
-    Range layer_range("moe/layer_forward");
-    Range stage("moe/route");
-    record(events ? events->before_route : nullptr, s);
-    RouteArgs ra{x, Wg, bias, idx, tw, d.T, d.H, d.E, d.k};
-    ra.renorm = gating ? (gating->renormalize != 0) : 1;
-    ra.err = err;
-    ra.logits = reinterpret_cast<float*>(w + L.logits);
-    if (plan.router == MOE_ROUTER_TENSOR)
-        MOE_TRY(launch_route_tc(ra, tc_args_of(L, w), sms, s));
-    else
-        MOE_TRY(launch_route(ra, sms, s));
-
-    stage.next("moe/permute");
-    record(events ? events->before_permute : nullptr, s);
-    PermuteArgs pa{idx, counts, offsets, src, inv, tile, reinterpret_cast<int32_t*>(w + L.hist), err,
-                   R, d.E};
-    MOE_TRY(launch_permute(pa, s));
-
-    const bool permuted = (plan.gemm0_a == MOE_GEMM0_A_PERMUTED);
-    const bool cp_gather = (plan.gemm0_a == MOE_GEMM0_A_CP_GATHER);
-    uint16_t* xp = reinterpret_cast<uint16_t*>(w + L.xp);
-    // x_perm: copied by GEMM0's copy warps while it runs, or by a kernel first
-    const bool copy_inline = permuted && plan.x_perm_copy == MOE_X_PERM_COPY_INLINE;
-    if (permuted && !copy_inline)
-        MOE_TRY(launch_scatter_rows(x, idx, inv, offsets + d.E, xp, d.T, d.H, d.k, d.E, err, sms, s));
-
-    // both routed GEMMs in one launch (dense A only)
-    const bool fuse_gemms = plan.gemm_fusion == MOE_GEMM_FUSION_ON;
-
-    stage.next("moe/experts");
-    record(events ? events->before_gemm0 : nullptr, s);
-    MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)R, d.F, d.E, d.k, x, permuted ? xp : nullptr, src,
-                                    tile, offsets, W1, W3, W2, tw, slot,
-                                    reinterpret_cast<uint16_t*>(w + L.h), err, sms, s,
-                                    events ? events->before_gemm1 : nullptr,
-                                    // with a shared expert, only its GEMM1 (the last) combines
-                                    FusedCombine{fused && d.F_shared == 0, 0, n_slots, arrive, out}, cp_gather,
-                                    fuse_gemms ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr,
-                                    plan.cta_group, plan.cta_group_gemm1,
-                                    copy_inline ? reinterpret_cast<int32_t*>(w + L.ready) : nullptr,
-                                    copy_inline ? xp : nullptr));
-
-    stage.next("moe/shared_expert");
-    record(events ? events->before_shared : nullptr, s);
-    if (d.F_shared > 0) {
-        // the sigmoid gate, if any, is the shared expert's row weight in GEMM1
-        float* sgate = nullptr;
-        if (shared_gate) {
-            sgate = reinterpret_cast<float*>(w + L.sgate);
-            MOE_TRY(launch_shared_gate(x, shared_gate, sgate, d.T, d.H, sms, s));
-        }
-        // identity dispatch: every token, in token order, weight 1
-        MOE_TRY_STATUS(run_expert_gemms(d, (int32_t)d.T, d.F_shared, 1, 1, x,
-                                        (permuted || cp_gather) ? x : nullptr,
-                                        nullptr, nullptr, nullptr, W1s, W3s, W2s, sgate,
-                                        fused ? slot : slot + (size_t)d.k * d.T * d.H,
-                                        reinterpret_cast<uint16_t*>(w + L.hs), err, sms, s, nullptr,
-                                        // every routed slot is written: one arrival each
-                                        FusedCombine{fused, d.k, n_slots, arrive, out, 1}, false, nullptr,
-                                        (permuted || cp_gather) ? cta_group_for(d.T, 1, false) : 1,
-                                        cta_group_for(d.T, 1, true)));
-    }
-
-    stage.next("moe/combine");
-    record(events ? events->before_combine : nullptr, s);
-    if (!fused)   // else GEMM1's epilogue finished it (the last contribution)
-        MOE_TRY(launch_combine(slot, n_slots, out, d.T, d.H, sms, s));
-    record(events ? events->after_combine : nullptr, s);
-    return finish(cudaSuccess, ws, s);
+    return layer_forward_impl(dims, x, Wg, bias, gating, W1, W3, W2, W1s, W3s, W2s, out, routing, ws, ws_bytes,
+                              events, stream, -1);
 }
 
 int32_t moe_host_chunks(const moe_dims* dims)
@@ -848,6 +871,8 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const moe_bf16* x_host, 
     if (n_chunks < 0 || n_chunks > 64) return MOE_ERR_INVALID_ARG;
     Range range("moe/layer_forward_host");
     const int32_t n = n_chunks == 0 ? host_chunks_of(d) : n_chunks;
+    // every chunk takes the router family of the whole batch
+    const int batch_router = plan_of(d).router;
     // chunk c: tokens [c*base, min(T, (c+1)*base)), base a multiple of 128
     int64_t base = (d.T + n - 1) / n;
     base = (base + 127) / 128 * 128;
@@ -882,8 +907,9 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const moe_bf16* x_host, 
         moe_dims dc = d;
         dc.T = tc;
         MOE_TRY(cudaStreamWaitEvent(s, ev[2 + 2 * c], 0));
-        MOE_TRY_STATUS(moe_layer_forward_ex(&dc, x_dev + t0 * d.H, Wg, bias, nullptr, W1, W3, W2, W1s, W3s, W2s,
-                                            out_dev + t0 * d.H, nullptr, ws, ws_bytes, nullptr, stream));
+        MOE_TRY_STATUS(layer_forward_impl(&dc, x_dev + t0 * d.H, Wg, bias, nullptr, W1, W3, W2, W1s, W3s, W2s,
+                                          out_dev + t0 * d.H, nullptr, ws, ws_bytes, nullptr, stream,
+                                          batch_router));
         MOE_TRY(cudaEventRecord(ev[3 + 2 * c], s));
         MOE_TRY(cudaStreamWaitEvent(d2h, ev[3 + 2 * c], 0));
         MOE_TRY(cudaMemcpyAsync(out_host + t0 * d.H, out_dev + t0 * d.H, (size_t)tc * row, cudaMemcpyDeviceToHost,
