@@ -155,9 +155,14 @@ def roofline_stage_bytes(cfg):
         "route": T * H * 2 + H * E * 2 + T * k * 8,
         "combine": n_slots * T * H * 4 + T * H * 2,
         "permute_index": R * 4 * 4 + E * 8,
-        # the dispatch with x_perm materialised: each token's row of x read once,
-        # each routed row of x_perm written once, and the index arrays
-        "permute": T * H * 2 + R * H * 2 + R * 4 * 4,
+        # the dispatch with x_perm materialised, as the scope table defines it:
+        # every routed row read from x and written to x_perm
+        "permute": 2 * R * H * 2,
+        # the least a dispatch can move: each token's row of x read once, each
+        # routed row of x_perm written once, the index arrays (the token-side
+        # copy moves about this; it reads x once where the rows are read k times
+        # in the definition above, so that figure can exceed the copy bandwidth)
+        "permute_min": T * H * 2 + R * H * 2 + R * 4 * 4,
     }
 
 
@@ -351,8 +356,13 @@ def bench_ours(args, cfg):
     stage_roofline["route"]["frac"] = round(stage_roofline["route"]["gbs"] / peaks["hbm_gbs"], 4)
     if plan.x_perm_copy == lib.X_PERM_COPY_KERNEL:
         # index phases + the x_perm copy, against the copy's algorithmic bytes
-        gbs = by["permute"] / (np.mean(stage_ms["permute"]) * 1e-3) / 1e9
-        stage_roofline["permute"] = {"gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4)}
+        t_perm = np.mean(stage_ms["permute"]) * 1e-3
+        gbs = by["permute"] / t_perm / 1e9
+        gbs_min = by["permute_min"] / t_perm / 1e9
+        stage_roofline["permute"] = {"gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                     "bytes": "2*R*H*2 (routed rows read and written)",
+                                     "min_bytes_gbs": round(gbs_min, 1),
+                                     "min_bytes_frac": round(gbs_min / peaks["hbm_gbs"], 4)}
 
     value = world * flops / (ms * 1e-3) / 1e12
     fused = plan.combine == lib.COMBINE_FUSED
@@ -468,8 +478,9 @@ def bench_reference(args, cfg):
 def bench_stage(args):
     """One stage through the C ABI at any shape (--T --H --E --k), outside the
     layer call: `route` (moe_route; T*H*2 + H*E*2 + T*k*8 bytes) or `permute`
-    (moe_permute with x_perm; T*H*2 + T*k*H*2 + T*k*16 bytes: x read once, x_perm
-    written, the index arrays). Before every timed call L2 is
+    (moe_permute with x_perm; 2*T*k*H*2 bytes: the routed rows read and written,
+    and, as min_bytes, T*H*2 + T*k*H*2 + T*k*16: x read once, x_perm written, the
+    index arrays). Before every timed call L2 is
     emptied of the inputs by writing and then reading a 256 MiB buffer (the
     read leaves L2 holding clean lines, so the timed call pays no write-back
     of the flush); each call is timed with CUDA events on the current stream.
@@ -517,15 +528,19 @@ def bench_stage(args):
     if ws is not None and lib.check(ws) != lib.MOE_OK:
         raise RuntimeError("device error in the stage calls")
     t = float(np.median(times))
-    work = (T * H * 2 + H * E * 2 + T * k * 8 if args.stage == "route"
-            else T * H * 2 + T * k * H * 2 + T * k * 4 * 4)
+    work = T * H * 2 + H * E * 2 + T * k * 8 if args.stage == "route" else 2 * T * k * H * 2
+    work_min = None if args.stage == "route" else T * H * 2 + T * k * H * 2 + T * k * 4 * 4
     peaks = measured_peaks()
     gbs = work / t / 1e9
-    return {"stage": args.stage, "config": {"T": T, "H": H, "E": E, "k": k},
+    line = {"stage": args.stage, "config": {"T": T, "H": H, "E": E, "k": k},
             "us_median": round(t * 1e6, 2), "us_min": round(min(times) * 1e6, 2),
             "algorithmic_bytes": work, "gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
             "peak_source": f"{peaks['source']} HBM copy bandwidth (MEASURED_PEAKS.json)",
             "steps": args.steps, "warmup": args.warmup}
+    if work_min is not None:
+        line.update(min_bytes=work_min, min_bytes_gbs=round(work_min / t / 1e9, 1),
+                    min_bytes_frac=round(work_min / t / 1e9 / peaks["hbm_gbs"], 4))
+    return line
 
 
 def main():
