@@ -113,6 +113,44 @@ def test_host_entry_validation_without_launch(L):
                                     null, null, null, 0, ws, lib.workspace_size(d0), null) == 0
 
 
+def test_nvtx_range_recorded(tmp_path):
+    """The library's NVTX ranges reach a tool: a small NVTX tool library
+    (tests/nvtx_recorder.c, loaded through NVTX_INJECTION64_PATH) records the
+    pushes and pops of a child process whose host-buffer call opens its range
+    and returns (no device here) with the range closed."""
+    import shutil
+    import subprocess
+    import sys
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("the call would run on a GPU; this test wants it to stop at the first CUDA call")
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    from token_dispatch_grouped_moe_gb300 import build
+    build.build()
+    tool = tmp_path / "libnvtx_recorder.so"
+    inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    subprocess.run([cc, "-shared", "-fPIC", "-O1", "-I", inc, os.path.join(ROOT, "tests", "nvtx_recorder.c"),
+                    "-o", str(tool)], check=True)
+    log = tmp_path / "nvtx.log"
+    child = (
+        "import ctypes, sys\n"
+        f"sys.path.insert(0, {ROOT!r})\n"
+        "from token_dispatch_grouped_moe_gb300 import lib\n"
+        "L = lib.load()\n"
+        "d = lib.make_dims(1000, 64, 64, 8, 2)\n"
+        "p = ctypes.c_void_p(256)\n"
+        "st = L.moe_layer_forward_host(ctypes.byref(d), p, p, None, p, p, p, None, None, None, p, p, p, 0,\n"
+        "                              ctypes.c_void_p(4096), lib.workspace_size(d), None)\n"
+        "print(st)\n")
+    env = dict(os.environ, NVTX_INJECTION64_PATH=str(tool), MOE_NVTX_LOG=str(log))
+    r = subprocess.run([sys.executable, "-c", child], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == "4"   # MOE_ERR_CUDA: no device behind the first CUDA call
+    assert log.read_text().splitlines() == ["push moe/layer_forward_host", "pop"]
+
+
 def test_host_chunks_table(L):
     """The library's chunk count: >= 8192 tokens a chunk, at most three."""
     from token_dispatch_grouped_moe_gb300 import lib
