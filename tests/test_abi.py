@@ -210,9 +210,9 @@ def test_layer_plan_table(L):
     want = {   # config: (router, combine, gemm_fusion, CTAs per MMA of GEMM0 and of GEMM1)
         "tiny": (lib.ROUTER_STREAM, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON, 1, 1),
         "mixtral": (lib.ROUTER_STREAM, lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF, 2, 2),
-        "qwen2": (lib.ROUTER_SLICED, lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF, 1, 2),
+        "qwen2": (lib.ROUTER_TENSOR, lib.COMBINE_FUSED, lib.GEMM_FUSION_OFF, 1, 2),
         "dsk-1k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON, 1, 1),
-        "dsk-4k": (lib.ROUTER_SLICED, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON, 1, 1),
+        "dsk-4k": (lib.ROUTER_TENSOR, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_ON, 1, 1),
         "dsk-16k": (lib.ROUTER_TENSOR, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_OFF, 2, 2),
         "dsk-32k": (lib.ROUTER_TENSOR, lib.COMBINE_SEPARATE, lib.GEMM_FUSION_OFF, 2, 2),
     }
@@ -256,10 +256,10 @@ def test_layer_plan_table(L):
     assert lib.layer_plan(lib.make_dims(64, 256, 64, 196, 2)).router == lib.ROUTER_BLOCK
     assert lib.layer_plan(lib.make_dims(64, 16384, 64, 8, 2)).router == lib.ROUTER_BLOCK
     # the tensor-core router by default for 16 <= E <= 64 (a multiple of 8)
-    # from 8192 tokens; forced by the option from 512 tokens and E >= 8; the
+    # from 4096 tokens; forced by the option from 512 tokens and E >= 8; the
     # other option value keeps the FMA routers
-    assert lib.layer_plan(lib.make_dims(8192, 256, 64, 64, 6)).router == lib.ROUTER_TENSOR
-    assert lib.layer_plan(lib.make_dims(8191, 256, 64, 64, 6)).router == lib.ROUTER_SLICED
+    assert lib.layer_plan(lib.make_dims(4096, 256, 64, 64, 6)).router == lib.ROUTER_TENSOR
+    assert lib.layer_plan(lib.make_dims(4095, 256, 64, 64, 6)).router == lib.ROUTER_SLICED
     assert lib.layer_plan(lib.make_dims(65536, 4096, 64, 8, 2)).router == lib.ROUTER_STREAM
     assert lib.layer_plan(lib.make_dims(16384, 256, 64, 12, 2)).router == lib.ROUTER_CLUSTER
     assert lib.layer_plan(lib.make_dims(16384, 256, 64, 72, 2)).router == lib.ROUTER_SLICED

@@ -164,13 +164,14 @@ moe_plan plan_of(const moe_dims& d)
     const int router_opt = g_router.load();
     // the tensor-core router (the ids are the same either way): forced by the
     // option wherever it applies, else where it measured faster than the FMA
-    // routers on GB300: E >= 16 from 8192 tokens (DeepSeek-shaped T = 16384:
-    // 107 -> 63 us, T = 32768: 206 -> 104 us). Below that, and for E = 8, the
-    // FMA routers are as fast or faster (Mixtral-shaped 27 vs 52 us, Qwen2-
-    // shaped 64 vs 69 us, DeepSeek-shaped T = 1024 26 vs 43 us).
+    // routers on GB300: E >= 16 from 4096 tokens (DeepSeek-shaped T = 4096:
+    // 44 -> 36 us, T = 16384: 107 -> 55 us, T = 32768: 206 -> 83 us; Qwen2-
+    // shaped T = 4096: 68 -> 60 us). Below that, and for E = 8, the FMA
+    // routers are as fast or faster (Mixtral-shaped 27 vs 45 us, DeepSeek-
+    // shaped T = 1024 26 vs 36 us).
     if (route_tc_supported(d.T, d.H, d.E) &&
         (router_opt == MOE_ROUTER_OPT_TENSOR ||
-         (router_opt == MOE_ROUTER_OPT_AUTO && d.E >= 16 && d.T >= 8192)))
+         (router_opt == MOE_ROUTER_OPT_AUTO && d.E >= 16 && d.T >= 4096)))
         p.router = MOE_ROUTER_TENSOR;
     p.gemm0_a = g_gemm0_a.load();
     const int combine_opt = g_combine.load();

@@ -38,7 +38,9 @@
 //      with a tolerance).
 //   5. Otherwise only the ambiguous runs are recomputed in the canonical order
 //      (lane L = canonical lane L, fmaf in increasing h, the butterfly) by
-//      the token's warp: the positions whose gap to a neighbour is at most
+//      the fix kernel (a warp per listed token, or below 8192 tokens a block
+//      whose warps share its run members): the positions whose gap to a
+//      neighbour is at most
 //      2 B_t, the run at the k / k+1 boundary extended by every expert within
 //      2 B_t below it (chained). Each run is more than 2 B_t away from every
 //      other expert, so ordering run members by their canonical logits and
@@ -64,6 +66,14 @@ constexpr int kTcThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int kTcABytes = kTcTile * kTcBK * 2;   // 16 KB
 constexpr int kTcPartKB = 1;      // k-blocks per TMEM partial (4 MMAs of K = 16)
 constexpr int kTcPrepRows = 64;   // gate rows per block of the prep kernel
+constexpr int kSelectThreads = 128;   // the striding select kernel: 4 warps of 4 tokens per block
+constexpr int kFixThreads = 128;      // the block fix kernel: 4 warps per listed token
+// From this many tokens the select and fix steps take a warp per group and a
+// warp per listed token (many listed tokens, short member lists); below, the
+// striding select kernel and a block per listed token (measured on GB300,
+// DeepSeek-shaped E = 64: T = 4096 route 44 -> 36 us, T = 32768 83 -> 110 us
+// the other way round).
+constexpr int64_t kTcManyTokens = 8192;
 
 // A stage holds the x tile (128 token rows x 64 of H) and the gate tile (NP
 // expert rows x 64 of H), both K-major in 128-byte-swizzled rows; one MMA per
@@ -454,15 +464,13 @@ __device__ __forceinline__ void canonical_pair(const uint16_t* xrow, const uint1
 // other expert: each run is separated from the rest by more than 2 B_t, so
 // this order is the canonical one.
 template <int PMAX>
-__global__ void __launch_bounds__(256) route_tc_select_kernel(const RouteArgs a, const RouteTcArgs c)
+__device__ __forceinline__ void select_group(const RouteArgs& a, const RouteTcArgs& c, int64_t grp)
 {
-    pdl_wait();
-    pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31;
     const int r = lane & 7, sub = lane >> 3;
     const int E = a.E, k = a.k;
     const int per = E >> 3;
-    const int64_t t = ((int64_t)blockIdx.x * 8 + warp) * 4 + sub;
+    const int64_t t = grp * 4 + sub;
     const bool live = t < a.T;
     const int e_lo = r * per;
     const unsigned gmask = 0xFFu << (8 * sub);
@@ -565,7 +573,7 @@ __global__ void __launch_bounds__(256) route_tc_select_kernel(const RouteArgs a,
             }
         }
     }
-    // list the token: its runs and its top list, for route_tc_fix_kernel
+    // list the token: its runs and its top list, for the fix kernel
     if (need && r == 0) {
         const int slot = atomicAdd(c.n_exact, 1);
         c.flag_tok[slot] = (int32_t)t;
@@ -578,11 +586,136 @@ __global__ void __launch_bounds__(256) route_tc_select_kernel(const RouteArgs a,
     }
 }
 
-// One warp per listed token: the canonical logits of its run members (two
-// experts per pass), then lane 0 orders the top list and the run members
-// below it (canonical logits for run members, fast logits otherwise) and
-// writes the k ids and weights.
-__global__ void __launch_bounds__(256) route_tc_fix_kernel(const RouteArgs a, const RouteTcArgs c)
+// Four tokens per warp (select_group), one group per warp: from 8192 tokens.
+template <int PMAX>
+__global__ void __launch_bounds__(256) route_tc_select_kernel(const RouteArgs a, const RouteTcArgs c)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    select_group<PMAX>(a, c, (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5));
+}
+
+// Below 8192 tokens: the warps of a grid sized to the resident blocks stride
+// over the groups, so the selection runs in one wave.
+template <int PMAX>
+__global__ void __launch_bounds__(kSelectThreads) route_tc_select_stride_kernel(const RouteArgs a,
+                                                                                const RouteTcArgs c)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t n_groups = (a.T + 3) / 4;
+    const int64_t warps = (int64_t)gridDim.x * (kSelectThreads / 32);
+    for (int64_t grp = (int64_t)blockIdx.x * (kSelectThreads / 32) + (threadIdx.x >> 5); grp < n_groups; grp += warps)
+        select_group<PMAX>(a, c, grp);
+}
+
+// Below 8192 tokens, a block per listed token: its warps share the run
+// members (warp w takes the pairs w, w + 4, ... of the member list; each
+// pair's canonical logits by the whole warp, two experts per pass), then
+// thread 0 orders the top list and the run members below it (canonical
+// logits for run members, fast logits otherwise) and writes the k ids and
+// weights. A token's members thus cost about one pass, not one per pair.
+__global__ void __launch_bounds__(kFixThreads) route_tc_fix_block_kernel(const RouteArgs a, const RouteTcArgs c)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    __shared__ float lg[64];
+    __shared__ int mem_s[64];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n = *c.n_exact;
+    const int E = a.E, k = a.k;
+    const int kk1 = k < E ? k + 1 : E;
+    for (int i = blockIdx.x; i < n; i += gridDim.x) {
+        const int64_t t = c.flag_tok[i];
+        const uint64_t cm = c.flag_cand[i];
+        // the members in increasing id order
+        int n_mem = 0;
+        if (threadIdx.x == 0) {
+            uint64_t rest = cm;
+            while (rest) {
+                mem_s[n_mem++] = __ffsll((long long)rest) - 1;
+                rest &= rest - 1;
+            }
+        }
+        n_mem = __popcll((long long)cm);
+        __syncthreads();
+        const uint16_t* xrow = a.x + t * a.H;
+        for (int q = 2 * warp; q < n_mem; q += 2 * (kFixThreads / 32)) {
+            const int e0 = mem_s[q];
+            const int e1 = q + 1 < n_mem ? mem_s[q + 1] : -1;
+            float l0, l1;
+            canonical_pair(xrow, c.wgt, a.H, e0, e1, lane, l0, l1);
+            if (lane == 0) {
+                lg[e0] = a.bias ? l0 + a.bias[e0] : l0;
+                if (e1 >= 0) lg[e1] = a.bias ? l1 + a.bias[e1] : l1;
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float key[9];
+            int id[9];
+            for (int j = 0; j < kk1; ++j) {
+                id[j] = c.flag_sel[(int64_t)i * 9 + j];
+                key[j] = c.flag_selv[(int64_t)i * 9 + j];
+            }
+            uint64_t extra = cm;
+            for (int j = 0; j < kk1; ++j) {
+                if ((cm >> id[j]) & 1ull) key[j] = lg[id[j]];
+                extra &= ~(1ull << id[j]);
+            }
+            int osel[8];
+            float ov[8];
+            uint32_t used = 0;
+            uint64_t used_x = 0;
+            for (int j = 0; j < k; ++j) {
+                float bv = 0.0f;
+                int be = -1, bi = -1;
+                for (int q = 0; q < kk1; ++q)
+                    if (!((used >> q) & 1u) && (be < 0 || key[q] > bv || (key[q] == bv && id[q] < be))) {
+                        bv = key[q];
+                        be = id[q];
+                        bi = q;
+                    }
+                uint64_t rx = extra & ~used_x;
+                while (rx) {
+                    const int e = __ffsll((long long)rx) - 1;
+                    rx &= rx - 1;
+                    if (be < 0 || lg[e] > bv || (lg[e] == bv && e < be)) {
+                        bv = lg[e];
+                        be = e;
+                        bi = 64 + e;
+                    }
+                }
+                if (bi >= 64) used_x |= 1ull << (bi - 64); else used |= 1u << bi;
+                osel[j] = be;
+                ov[j] = bv;
+            }
+            const float m0 = ov[0];
+            float ex[8], den = 0.0f;
+            for (int j = 0; j < k; ++j) {
+                ex[j] = expf(ov[j] - m0);
+                den = den + ex[j];
+            }
+            if (!a.renorm) {
+                // every expert is a run member here: canonical logits throughout
+                den = 0.0f;
+                for (int e = 0; e < E; ++e) den = den + expf(lg[e] - m0);
+            }
+            for (int j = 0; j < k; ++j) {
+                a.topk_idx[t * k + j] = osel[j];
+                a.topk_w[t * k + j] = ex[j] / den;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// The fix step with one warp per listed token (from 8192 tokens, where many
+// tokens are listed and most have short member lists): the canonical logits
+// of its run members (two experts per pass), then lane 0 orders the top list
+// and the run members below it (canonical logits for run members, fast
+// logits otherwise) and writes the k ids and weights.
+__global__ void __launch_bounds__(256) route_tc_fix_warp_kernel(const RouteArgs a, const RouteTcArgs c)
 {
     pdl_wait();
     pdl_launch_dependents();
@@ -748,11 +881,28 @@ cudaError_t launch_route_tc(const RouteArgs& a, RouteTcArgs c, int num_sms, cuda
     else if (NP == 64) err = launch_tc<64>(a, c, num_sms, s);
     else return cudaErrorInvalidValue;
     if (err != cudaSuccess) return err;
-    const dim3 blocks((unsigned)((a.T + 31) / 32));   // 8 warps x 4 tokens
-    err = a.E <= 32 ? launch_pdl(route_tc_select_kernel<4>, blocks, dim3(256), 0, s, a, c)
-                    : launch_pdl(route_tc_select_kernel<8>, blocks, dim3(256), 0, s, a, c);
+    if (a.T >= kTcManyTokens) {
+        // many tokens: a warp per 4-token group, then a warp per listed token
+        const dim3 blocks((unsigned)((a.T + 31) / 32));   // 8 warps x 4 tokens
+        err = a.E <= 32 ? launch_pdl(route_tc_select_kernel<4>, blocks, dim3(256), 0, s, a, c)
+                        : launch_pdl(route_tc_select_kernel<8>, blocks, dim3(256), 0, s, a, c);
+        if (err != cudaSuccess) return err;
+        return launch_pdl(route_tc_fix_warp_kernel, dim3((unsigned)(8 * num_sms)), dim3(256), 0, s, a, c);
+    }
+    // fewer: the resident blocks stride over the groups (one wave), then a
+    // block per listed token
+    auto sel = a.E <= 32 ? route_tc_select_stride_kernel<4> : route_tc_select_stride_kernel<8>;
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sel, kSelectThreads, 0);
     if (err != cudaSuccess) return err;
-    return launch_pdl(route_tc_fix_kernel, dim3((unsigned)(8 * num_sms)), dim3(256), 0, s, a, c);
+    const int64_t need = (a.T + 4 * (kSelectThreads / 32) - 1) / (4 * (kSelectThreads / 32));
+    const int64_t resident = (int64_t)num_sms * (per_sm > 0 ? per_sm : 1);
+    err = launch_pdl(sel, dim3((unsigned)(need < resident ? need : resident)), dim3(kSelectThreads), 0, s, a, c);
+    if (err != cudaSuccess) return err;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_tc_fix_block_kernel, kFixThreads, 0);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(route_tc_fix_block_kernel, dim3((unsigned)(num_sms * (per_sm > 0 ? per_sm : 1))),
+                      dim3(kFixThreads), 0, s, a, c);
 }
 
 }  // namespace moe
