@@ -205,7 +205,8 @@ size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct Layout {
     size_t err, tile, hist, idx, w, counts, offsets, src, inv, xp, h, hs, slot, arrive, sgate, logits, ready;
-    size_t tc_wgt, tc_wnorm, tc_nflag, tc_tok, tc_cand, tc_ftok, tc_fcand, tc_fsel, tc_fselv, total;
+    size_t tc_wgt, tc_wnorm, tc_nflag, tc_tok, tc_cand, tc_ftok, tc_fcand, tc_fsel, tc_fselv, tc_pairs, tc_lg,
+        total;
 };
 
 Layout layout_of(const moe_dims& d)
@@ -244,6 +245,8 @@ Layout layout_of(const moe_dims& d)
     L.tc_fcand = o; o += al256(tc ? T * 8 : 0);
     L.tc_fsel = o; o += al256(tc ? T * 9 * 4 : 0);
     L.tc_fselv = o; o += al256(tc ? T * 9 * 4 : 0);
+    L.tc_pairs = o; o += al256(tc ? T * 32 * 4 : 0);                // (token, member pair) items
+    L.tc_lg = o; o += al256(tc ? T * 64 * 4 : 0);                   // their canonical logits
     L.total = o;
     return L;
 }
@@ -311,6 +314,8 @@ RouteTcArgs tc_args_of(const Layout& L, unsigned char* w)
     c.flag_cand = reinterpret_cast<uint64_t*>(w + L.tc_fcand);
     c.flag_sel = reinterpret_cast<int32_t*>(w + L.tc_fsel);
     c.flag_selv = reinterpret_cast<float*>(w + L.tc_fselv);
+    c.pairs = reinterpret_cast<int32_t*>(w + L.tc_pairs);
+    c.lg_buf = reinterpret_cast<float*>(w + L.tc_lg);
     return c;
 }
 

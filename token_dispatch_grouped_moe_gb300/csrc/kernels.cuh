@@ -51,7 +51,9 @@ struct RouteTcArgs {
     float* wpart;           // [H/64, NP] sums of squares of the gate's columns per 64 rows, rounded up
     float* fast;            // [T, E] the tensor-core logits (bias added)
     float* bound;           // [T] B_t: |fast - canonical| <= B_t for every expert of token t
-    int32_t* n_exact;       // tokens listed for the canonical recomputation (a count)
+    int32_t* n_exact;       // [2] tokens listed for the canonical recomputation, their member pairs
+    int32_t* pairs = nullptr;   // [32 T] listed (token slot * 32 + pair) work items, or null
+    float* lg_buf = nullptr;    // [T, 64] canonical logits of the listed tokens' run members
     int32_t* flag_tok;      // [T] the listed tokens
     uint64_t* flag_cand;    // [T] their run members (bit e)
     int32_t* flag_sel;      // [T, 9] their top k+1 by fast logit

@@ -165,7 +165,7 @@ __global__ void __launch_bounds__(256) route_tc_prep_kernel(const uint16_t* __re
             }
         wpart[(int64_t)blockIdx.x * NP + e] = ss;
     }
-    if (blockIdx.x == 0 && threadIdx.x == 0) *n_exact = 0;
+    if (blockIdx.x == 0 && threadIdx.x < 2) n_exact[threadIdx.x] = 0;   // listed tokens, listed pairs
 }
 
 // ------------------------------------------------------------------ main --
@@ -583,6 +583,12 @@ __device__ __forceinline__ void select_group(const RouteArgs& a, const RouteTcAr
             c.flag_sel[(int64_t)slot * 9 + j] = sel[j];
             c.flag_selv[(int64_t)slot * 9 + j] = selv[j];
         }
+        if (c.pairs) {
+            // its (token, member pair) work items for the pairs kernel
+            const int np = (__popcll((long long)cand) + 1) >> 1;
+            const int pb = atomicAdd(c.n_exact + 1, np);
+            for (int q = 0; q < np; ++q) c.pairs[pb + q] = slot * 32 + q;
+        }
     }
 }
 
@@ -607,6 +613,69 @@ __global__ void __launch_bounds__(kSelectThreads) route_tc_select_stride_kernel(
     const int64_t warps = (int64_t)gridDim.x * (kSelectThreads / 32);
     for (int64_t grp = (int64_t)blockIdx.x * (kSelectThreads / 32) + (threadIdx.x >> 5); grp < n_groups; grp += warps)
         select_group<PMAX>(a, c, grp);
+}
+
+// The final order of one recomputed token (one thread): the top list (ids,
+// fast logits; the run members among them take their canonical logits from
+// lg) and the run members below it (canonical logits), ties to the lower id;
+// writes the k ids and weights (without renormalisation every expert is a
+// run member, so the denominator runs over canonical logits throughout).
+__device__ __forceinline__ void order_token(const RouteArgs& a, int64_t t, uint64_t cm, const int* id0,
+                                            const float* key0, int kk1, const float* lg)
+{
+    const int E = a.E, k = a.k;
+    float key[9];
+    int id[9];
+    for (int j = 0; j < kk1; ++j) {
+        id[j] = id0[j];
+        key[j] = key0[j];
+    }
+    uint64_t extra = cm;
+    for (int j = 0; j < kk1; ++j) {
+        if ((cm >> id[j]) & 1ull) key[j] = lg[id[j]];
+        extra &= ~(1ull << id[j]);
+    }
+    int osel[8];
+    float ov[8];
+    uint32_t used = 0;
+    uint64_t used_x = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = 0.0f;
+        int be = -1, bi = -1;
+        for (int q = 0; q < kk1; ++q)
+            if (!((used >> q) & 1u) && (be < 0 || key[q] > bv || (key[q] == bv && id[q] < be))) {
+                bv = key[q];
+                be = id[q];
+                bi = q;
+            }
+        uint64_t rx = extra & ~used_x;
+        while (rx) {
+            const int e = __ffsll((long long)rx) - 1;
+            rx &= rx - 1;
+            if (be < 0 || lg[e] > bv || (lg[e] == bv && e < be)) {
+                bv = lg[e];
+                be = e;
+                bi = 64 + e;
+            }
+        }
+        if (bi >= 64) used_x |= 1ull << (bi - 64); else used |= 1u << bi;
+        osel[j] = be;
+        ov[j] = bv;
+    }
+    const float m0 = ov[0];
+    float ex[8], den = 0.0f;
+    for (int j = 0; j < k; ++j) {
+        ex[j] = expf(ov[j] - m0);
+        den = den + ex[j];
+    }
+    if (!a.renorm) {
+        den = 0.0f;
+        for (int e = 0; e < E; ++e) den = den + expf(lg[e] - m0);
+    }
+    for (int j = 0; j < k; ++j) {
+        a.topk_idx[t * k + j] = osel[j];
+        a.topk_w[t * k + j] = ex[j] / den;
+    }
 }
 
 // Below 8192 tokens, a block per listed token: its warps share the run
@@ -710,107 +779,49 @@ __global__ void __launch_bounds__(kFixThreads) route_tc_fix_block_kernel(const R
     }
 }
 
-// The fix step with one warp per listed token (from 8192 tokens, where many
-// tokens are listed and most have short member lists): the canonical logits
-// of its run members (two experts per pass), then lane 0 orders the top list
-// and the run members below it (canonical logits for run members, fast
-// logits otherwise) and writes the k ids and weights.
-__global__ void __launch_bounds__(256) route_tc_fix_warp_kernel(const RouteArgs a, const RouteTcArgs c)
+// From 8192 tokens the fix step is balanced over (listed token, pair of run
+// members) work items, which the select kernel lists: a warp per item
+// computes the pair's canonical logits into lg_buf[token slot][expert], so a
+// token with a long member list spreads over several warps; then
+// route_tc_order_kernel finishes each token.
+__global__ void __launch_bounds__(256) route_tc_pairs_kernel(const RouteArgs a, const RouteTcArgs c)
 {
     pdl_wait();
     pdl_launch_dependents();
-    __shared__ float lg_s[8][64];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n = *c.n_exact;
-    const int E = a.E, k = a.k;
-    const int kk1 = k < E ? k + 1 : E;
-    float* lg = lg_s[warp];
-    for (int i = blockIdx.x * 8 + warp; i < n; i += gridDim.x * 8) {
+    const int lane = threadIdx.x & 31;
+    const int n_pairs = c.n_exact[1];
+    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < n_pairs; w += warps) {
+        const int ent = c.pairs[w];
+        const int i = ent >> 5, q = ent & 31;   // token slot, pair of its members
         const int64_t t = c.flag_tok[i];
-        const uint64_t cm = c.flag_cand[i];
-        // the token's top list, one entry per lane (gathered to lane 0 below)
-        int my_id = 0;
-        float my_v = 0.0f;
-        if (lane < kk1) {
-            my_id = c.flag_sel[(int64_t)i * 9 + lane];
-            my_v = c.flag_selv[(int64_t)i * 9 + lane];
-        }
-        const uint16_t* xrow = a.x + t * a.H;
-        uint64_t rest = cm;
-        while (rest) {
-            const int e0 = __ffsll((long long)rest) - 1;
-            rest &= rest - 1;
-            int e1 = -1;
-            if (rest) {
-                e1 = __ffsll((long long)rest) - 1;
-                rest &= rest - 1;
-            }
-            float l0, l1;
-            canonical_pair(xrow, c.wgt, a.H, e0, e1, lane, l0, l1);
-            if (lane == 0) {
-                lg[e0] = a.bias ? l0 + a.bias[e0] : l0;
-                if (e1 >= 0) lg[e1] = a.bias ? l1 + a.bias[e1] : l1;
-            }
-        }
-        __syncwarp();
-        float key[9];
-        int id[9];
-#pragma unroll
-        for (int j = 0; j < 9; ++j) {
-            id[j] = __shfl_sync(0xffffffffu, my_id, j);
-            key[j] = __shfl_sync(0xffffffffu, my_v, j);
-        }
+        uint64_t m = c.flag_cand[i];
+        for (int u = 0; u < 2 * q; ++u) m &= m - 1;   // drop the members of the pairs before
+        const int e0 = __ffsll((long long)m) - 1;
+        m &= m - 1;
+        const int e1 = m ? __ffsll((long long)m) - 1 : -1;
+        float l0, l1;
+        canonical_pair(a.x + t * a.H, c.wgt, a.H, e0, e1, lane, l0, l1);
         if (lane == 0) {
-            uint64_t extra = cm;
-            for (int j = 0; j < kk1; ++j) {
-                if ((cm >> id[j]) & 1ull) key[j] = lg[id[j]];
-                extra &= ~(1ull << id[j]);
-            }
-            int osel[8];
-            float ov[8];
-            uint32_t used = 0;
-            uint64_t used_x = 0;
-            for (int j = 0; j < k; ++j) {
-                float bv = 0.0f;
-                int be = -1, bi = -1;
-                for (int q = 0; q < kk1; ++q)
-                    if (!((used >> q) & 1u) && (be < 0 || key[q] > bv || (key[q] == bv && id[q] < be))) {
-                        bv = key[q];
-                        be = id[q];
-                        bi = q;
-                    }
-                uint64_t rx = extra & ~used_x;
-                while (rx) {
-                    const int e = __ffsll((long long)rx) - 1;
-                    rx &= rx - 1;
-                    if (be < 0 || lg[e] > bv || (lg[e] == bv && e < be)) {
-                        bv = lg[e];
-                        be = e;
-                        bi = 64 + e;
-                    }
-                }
-                if (bi >= 64) used_x |= 1ull << (bi - 64); else used |= 1u << bi;
-                osel[j] = be;
-                ov[j] = bv;
-            }
-            const float m0 = ov[0];
-            float ex[8], den = 0.0f;
-            for (int j = 0; j < k; ++j) {
-                ex[j] = expf(ov[j] - m0);
-                den = den + ex[j];
-            }
-            if (!a.renorm) {
-                // every expert is a run member here: canonical logits throughout
-                den = 0.0f;
-                for (int e = 0; e < E; ++e) den = den + expf(lg[e] - m0);
-            }
-            for (int j = 0; j < k; ++j) {
-                a.topk_idx[t * k + j] = osel[j];
-                a.topk_w[t * k + j] = ex[j] / den;
-            }
+            float* lg = c.lg_buf + (int64_t)i * 64;
+            lg[e0] = a.bias ? l0 + a.bias[e0] : l0;
+            if (e1 >= 0) lg[e1] = a.bias ? l1 + a.bias[e1] : l1;
         }
-        __syncwarp();
     }
+}
+
+// A thread per listed token: its final order from the pairs kernel's logits.
+// Token i goes to block i mod gridDim.x, so a few thousand tokens spread over
+// every SM (the work per token is a short serial chain of dependent loads).
+__global__ void __launch_bounds__(64) route_tc_order_kernel(const RouteArgs a, const RouteTcArgs c)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int n = c.n_exact[0];
+    const int kk1 = a.k < a.E ? a.k + 1 : a.E;
+    for (int64_t i = blockIdx.x + (int64_t)gridDim.x * threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        order_token(a, c.flag_tok[i], c.flag_cand[i], c.flag_sel + i * 9, c.flag_selv + i * 9, kk1,
+                    c.lg_buf + i * 64);
 }
 
 // The fast-path constants: c_fast bounds |f - S| and c_tot |f - l| per unit
@@ -881,13 +892,17 @@ cudaError_t launch_route_tc(const RouteArgs& a, RouteTcArgs c, int num_sms, cuda
     else if (NP == 64) err = launch_tc<64>(a, c, num_sms, s);
     else return cudaErrorInvalidValue;
     if (err != cudaSuccess) return err;
+    if (a.T < kTcManyTokens) c.pairs = nullptr;   // the block fix kernel takes whole tokens
     if (a.T >= kTcManyTokens) {
-        // many tokens: a warp per 4-token group, then a warp per listed token
+        // many tokens: a warp per 4-token group (which lists the recomputed
+        // tokens' member pairs), a warp per listed pair, a thread per listed token
         const dim3 blocks((unsigned)((a.T + 31) / 32));   // 8 warps x 4 tokens
         err = a.E <= 32 ? launch_pdl(route_tc_select_kernel<4>, blocks, dim3(256), 0, s, a, c)
                         : launch_pdl(route_tc_select_kernel<8>, blocks, dim3(256), 0, s, a, c);
         if (err != cudaSuccess) return err;
-        return launch_pdl(route_tc_fix_warp_kernel, dim3((unsigned)(8 * num_sms)), dim3(256), 0, s, a, c);
+        err = launch_pdl(route_tc_pairs_kernel, dim3((unsigned)(8 * num_sms)), dim3(256), 0, s, a, c);
+        if (err != cudaSuccess) return err;
+        return launch_pdl(route_tc_order_kernel, dim3((unsigned)(8 * num_sms)), dim3(64), 0, s, a, c);
     }
     // fewer: the resident blocks stride over the groups (one wave), then a
     // block per listed token
