@@ -773,6 +773,11 @@ def test_layer_in_cuda_graph(lib, shape):
     ((300, 256, 192, 64, 6, 0), 6),
     # + the shared expert's two GEMMs; two routed GEMM launches (1050 rows per expert)
     ((2100, 448, 320, 4, 2, 640), 8),
+    # the tensor-core router below 8192 tokens (prep, main, striding select, block
+    # fix), dispatch, copy, two GEMM launches, separate combine
+    ((4096, 256, 128, 16, 2, 0), 9),
+    # from 8192 tokens (prep, main, select, member pairs, order), then the same five
+    ((8192, 256, 128, 16, 2, 0), 10),
 ])
 def test_launch_count(lib, shape, expected):
     """moe_launch_count counts exactly the kernels a layer call launches."""
