@@ -47,7 +47,10 @@ def _route(lib, x, Wg, k, bias=None, renormalize=True, force_exact=False, want_f
 # (T, H, E, k): every padded width NP = 16, 32, 48, 64, ragged token tails
 SHAPES = [(512, 256, 8, 2), (1000, 512, 16, 4), (777, 64, 24, 3), (3000, 2048, 32, 6),
           (600, 192, 40, 8), (1500, 1024, 48, 5), (700, 320, 56, 7), (2100, 2048, 64, 6),
-          (513, 3584, 64, 8), (640, 4096, 8, 8)]
+          (513, 3584, 64, 8), (640, 4096, 8, 8),
+          # from 8192 tokens the recomputation runs as (token, member pair) items and an
+          # order pass; without renormalisation every expert is a member (32 pairs)
+          (8200, 512, 64, 6), (8192, 256, 16, 4)]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -71,7 +74,8 @@ def test_route_tc_matches_oracle(lib, oracle, shape, variant):
           f"{n_exact} of {T} ({100.0 * n_exact / T:.2f}%)")
 
 
-@pytest.mark.parametrize("shape", [(2048, 4096, 8, 2), (2048, 2048, 64, 6), (1024, 3584, 64, 8)])
+@pytest.mark.parametrize("shape", [(2048, 4096, 8, 2), (2048, 2048, 64, 6), (1024, 3584, 64, 8),
+                                   (20480, 512, 64, 6)])   # more tiles than SMs: two CTAs of 4 stages per SM
 @pytest.mark.parametrize("inputs", ["randn", "wide_range"])
 def test_route_tc_fast_logit_bound(lib, shape, inputs):
     """The tensor-core logits lie within the bound the screening assumes for
@@ -134,7 +138,8 @@ def test_route_tc_order_sensitive(lib, oracle, E, case):
     assert n_exact >= 1
 
 
-@pytest.mark.parametrize("shape", [(1024, 2048, 64, 6), (2048, 4096, 8, 2), (600, 512, 24, 3)])
+@pytest.mark.parametrize("shape", [(1024, 2048, 64, 6), (2048, 4096, 8, 2), (600, 512, 24, 3),
+                                   (8192, 512, 64, 6), (9000, 256, 16, 3)])
 def test_route_tc_all_exact_equals_fma_router(lib, shape):
     """With every token sent through the canonical recomputation, the ids and
     weights equal the FMA router's (moe_route) bit for bit."""
