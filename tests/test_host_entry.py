@@ -46,7 +46,7 @@ CASES = [(1000, 256, 192, 8, 2, 0), (700, 256, 128, 16, 4, 256), (300, 128, 128,
 
 @pytest.mark.parametrize("n_chunks", [0, 2, 3])
 def test_host_call_keeps_the_batch_router(lib, n_chunks):
-    """A batch that takes the tensor-core router (E >= 16 from 8192 tokens)
+    """A batch that takes the tensor-core router (E >= 16 from 4096 tokens)
     in chunks of fewer tokens: each chunk still takes it, so the gate weights
     and the output are the whole batch's bit for bit."""
     T, H, F, E, k = 9000, 256, 128, 16, 2
