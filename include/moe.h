@@ -420,7 +420,8 @@ moe_status moe_layer_forward_ex(const moe_dims* dims, const moe_bf16* x, const m
  * once out_host holds the result (synchronize the stream before reading it).
  * Errors: the argument checks of moe_layer_forward (MOE_ERR_INVALID_ARG for
  * a null or misaligned pointer or n_chunks outside 0..64); MOE_ERR_CUDA if a
- * copy, an event or a launch fails, after which out_host is unspecified.
+ * copy, an event or a launch fails, after which out_host is unspecified (work
+ * queued on `stream` afterwards still waits for every copy already queued).
  * Concurrent calls from several host threads on one device share the copy
  * streams and are serialized by them (correct, not overlapped).
  */

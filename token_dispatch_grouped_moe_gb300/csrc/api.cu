@@ -897,6 +897,20 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const moe_bf16* x_host, 
     } release{ev};
     for (cudaEvent_t& e : ev) MOE_TRY(cudaEventCreateWithFlags(&e, cudaEventDisableTiming));
     cudaEvent_t ev_start = ev[0], ev_done = ev[1];
+    // on every return, also after a failure part way, later work on the
+    // caller's stream waits for every copy this call queued (so the caller may
+    // reuse its buffers once the stream has drained)
+    struct Join {
+        cudaStream_t s, h2d, d2h;
+        cudaEvent_t e_h2d, e_d2h;
+        bool armed = true;
+        ~Join()
+        {
+            if (!armed) return;
+            if (cudaEventRecord(e_h2d, h2d) == cudaSuccess) cudaStreamWaitEvent(s, e_h2d, 0);
+            if (cudaEventRecord(e_d2h, d2h) == cudaSuccess) cudaStreamWaitEvent(s, e_d2h, 0);
+        }
+    } join{s, h2d, d2h, ev_start, ev_done};   // (ev_start may be recorded again: earlier waits keep their record)
     // the copies start after the work already queued on the caller's stream
     MOE_TRY(cudaEventRecord(ev_start, s));
     MOE_TRY(cudaStreamWaitEvent(h2d, ev_start, 0));
@@ -922,6 +936,8 @@ moe_status moe_layer_forward_host(const moe_dims* dims, const moe_bf16* x_host, 
                                 d2h));
     }
     // later work on the caller's stream waits for the last copy to the host
+    // (the copies to the device are done: every chunk's layer call waited on them)
+    join.armed = false;
     MOE_TRY(cudaEventRecord(ev_done, d2h));
     MOE_TRY(cudaStreamWaitEvent(s, ev_done, 0));
     return finish(cudaSuccess, ws, s);
