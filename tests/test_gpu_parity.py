@@ -630,6 +630,38 @@ def _stage_api_matches_layer(lib):
     assert torch.equal(x_perm, g["x"][tok])
 
 
+@pytest.mark.parametrize("T,E,k,pattern", [
+    (1, 8, 1, "uniform"),
+    (33, 16, 3, "uniform"),
+    (1000, 64, 6, "skewed"),       # R = 6000: three chunks, the last part full
+    (1024, 8, 2, "uniform"),       # R = 2048: exactly one chunk, two full rounds
+    (1025, 8, 2, "uniform"),       # R = 2050: a second chunk of two assignments
+    (5461, 64, 6, "one_expert"),   # every id the same expert
+    (4097, 256, 8, "skewed"),      # R = 32776, E at its largest
+])
+def test_permute_forms_against_oracle(lib, oracle, T, E, k, pattern):
+    """The dispatch gives the oracle's stable counting sort bit for bit on
+    uniform, skewed and single-expert ids, with chunks of 2048 assignments and
+    rounds of 1024 that end exactly or part way."""
+    rng = np.random.default_rng(T * 131 + E)
+    if pattern == "uniform":
+        ids = rng.integers(0, E, (T, k))
+    elif pattern == "skewed":
+        p = 1.0 / np.arange(1, E + 1) ** 1.2
+        ids = rng.choice(E, (T, k), p=p / p.sum())
+    else:
+        ids = np.full((T, k), E - 1)
+    ids = ids.astype(np.int32)
+    dims = lib.make_dims(T, 64, 64, E, k)
+    ws = lib.workspace(dims)
+    got = lib.permute(dims, torch.from_numpy(ids).cuda(), ws)
+    torch.cuda.synchronize()
+    assert lib.check(ws) == lib.MOE_OK
+    want = oracle.permute(ids, E)
+    for name, a, b in zip(("counts", "offsets", "src_row", "inv_pos"), got[:4], want):
+        assert np.array_equal(a.cpu().numpy(), b), f"{name} differs from the oracle"
+
+
 def test_bad_expert_id_reported(lib):
     """An id outside [0, E) is reported through the device error word; the
     other assignments are still dispatched; nothing is written out of bounds."""
